@@ -1,0 +1,163 @@
+/*
+ * usm.h — C ABI of the GB300 (sm_103a) unstructured sparse matrix library.
+ *
+ * Operations from "Sparse GPU Kernels for Deep Learning" (Gale, Zaharia,
+ * Young, Elsen, SC 2020): SpMM and SDDMM on plain CSR matrices with
+ * unstructured, moderately sparse (70–98%) deep-learning sparsity, plus the
+ * row-swizzle load-balancing order.  Every entry point takes plain pointers
+ * and sizes; no C++ or framework type crosses this boundary.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Array arguments are DEVICE pointers owned by the caller.  The
+ *   library never allocates, frees or keeps a pointer after the call returns.
+ *   Scratch memory, where an operation needs it, is passed in by the caller
+ *   ("workspace"); its size comes from the matching *_workspace_bytes call.
+ * CSR.  row_offsets is int32[M+1] with row_offsets[0] = 0, non-decreasing,
+ *   row_offsets[M] = nnz; col_indices is int32[nnz], each row's indices
+ *   strictly increasing and in [0, K).  The library does not scan the CSR
+ *   (that would cost a pass over it); a CSR that breaks this contract gives
+ *   undefined results but never an out-of-bounds dense access, because every
+ *   column index is clamped into [0, K) before it addresses a dense operand.
+ * Dense operands.  Row-major with a leading dimension (elements per row).
+ *   Base pointers must be 16-byte aligned and ld·sizeof(element) a multiple
+ *   of 16 bytes, else USM_ERR_ALIGNMENT.
+ * Types.  usm_dtype names the INPUT element type (values and dense
+ *   operands).  Products and sums are always fp32.  Dense outputs are fp32.
+ * Asynchrony.  Calls enqueue work on `stream` (a cudaStream_t; NULL = the
+ *   legacy default stream) and return without synchronising, except
+ *   usm_poll_status.  Device-side failures (a bounded wait that timed out)
+ *   are recorded in a per-device status word read by usm_poll_status.
+ * Errors.  Every entry point returns USM_OK or a negative usm_status; none
+ *   throws, aborts or prints.  Argument checks run on the host before any
+ *   launch, so a rejected call touches no device memory.
+ * Threads.  Calls may be issued from several host threads; the status word
+ *   is shared by all calls on one device.
+ */
+#ifndef USM_H_
+#define USM_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum usm_dtype { USM_F32 = 0, USM_BF16 = 1 } usm_dtype;
+
+typedef enum usm_status {
+    USM_OK = 0,
+    USM_ERR_INVALID_ARG = -1, /* negative size, NULL pointer with nonzero size, bad enum */
+    USM_ERR_ALIGNMENT = -2,   /* dense pointer or leading dimension not 16-byte aligned */
+    USM_ERR_UNSUPPORTED = -3, /* shape outside the documented limits */
+    USM_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+    USM_ERR_TIMEOUT = -5,     /* a device-side bounded wait gave up (see usm_poll_status) */
+    USM_ERR_WORKSPACE = -6    /* workspace NULL or smaller than *_workspace_bytes */
+} usm_status;
+
+/*
+ * csr_spmm — sparse × dense product, C = A · B.
+ *
+ * Source: "Sparse GPU Kernels for Deep Learning", summary card, "Summary"
+ * (SpMM on plain CSR with unstructured sparsity; the sparse layer's forward
+ * pass, and its input gradient when A is the transposed weight).
+ *
+ *   A : M×K sparse, CSR (row_offsets, col_indices, values[nnz] of `dtype`).
+ *   B : K×N dense, row-major, leading dimension ldb ≥ N, elements of `dtype`.
+ *   C : M×N dense fp32, row-major, leading dimension ldc ≥ N.  OVERWRITTEN:
+ *       C[r][j] = Σ_{p in row r} values[p] · B[col_indices[p]][j]
+ *       (rows of A with no nonzeros give zero rows of C).
+ *   row_swizzle : NULL, or int32[M], a permutation of 0..M-1 giving the order
+ *       in which rows are scheduled (see row_swizzle_build).  It changes only
+ *       the schedule, never the result (each output row is computed by one
+ *       unit in a fixed order).
+ * Limits: 0 ≤ M, K, N < 2^31, nnz < 2^31; ldc a multiple of 4.
+ * Empty cases: M = 0 or N = 0 is a no-op; nnz = 0 zero-fills C.
+ */
+int csr_spmm(int M, int K, int N, int nnz,
+             const int *row_offsets, const int *col_indices, const void *values,
+             const int *row_swizzle,
+             const void *B, int ldb,
+             float *C, int ldc,
+             usm_dtype dtype, void *stream);
+
+/*
+ * csr_sddmm — sampled dense–dense product on the mask of A.
+ *
+ * Source: "Sparse GPU Kernels for Deep Learning", summary card, "Interesting
+ * ideas" I3: the specialised form drops the element-wise scaling by A's
+ * values and takes the second operand transposed, the form weight gradients
+ * and sparse-attention scores need.
+ *
+ *   mask : M×K, CSR (row_offsets, col_indices); values are not read.
+ *   X    : M×D dense, row-major, leading dimension ldx ≥ D, `in_dtype`.
+ *   Y    : K×D dense, row-major, leading dimension ldy ≥ D, `in_dtype`
+ *          (used transposed: the product is X·Yᵀ).
+ *   out  : [nnz] in the mask's CSR order, element type `out_dtype`
+ *          (USM_F32, or USM_BF16 rounded to nearest even from the fp32 sum):
+ *          out[p] = Σ_{j<D} X[r][j] · Y[col_indices[p]][j],  p in row r.
+ *   row_swizzle : NULL or a permutation of 0..M-1 (schedule only).
+ *   workspace : device scratch of at least
+ *          csr_sddmm_workspace_bytes(M, K, D, nnz, in_dtype) bytes; may be
+ *          NULL when that size is 0.  Its contents on entry are ignored.
+ * Limits: as csr_spmm.  nnz = 0 or M = 0 is a no-op; D = 0 zero-fills out.
+ */
+size_t csr_sddmm_workspace_bytes(int M, int K, int D, int nnz, usm_dtype in_dtype);
+
+int csr_sddmm(int M, int K, int D, int nnz,
+              const int *row_offsets, const int *col_indices,
+              const int *row_swizzle,
+              const void *X, int ldx,
+              const void *Y, int ldy,
+              void *out, usm_dtype in_dtype, usm_dtype out_dtype,
+              void *workspace, size_t workspace_bytes,
+              void *stream);
+
+/*
+ * row_swizzle_build — the row-swizzle processing order.
+ *
+ * Source: "Sparse GPU Kernels for Deep Learning", summary card, "Summary"
+ * (a decoupled load-balancing scheme) and "Interesting ideas" I4 (row
+ * swizzle balances work independently of how the computation is split).
+ * Reading used here: rows are listed by decreasing length, rows of equal
+ * length by increasing index, so the permutation is unique.  With
+ * seg_rows > 0 the order is built separately inside each run of seg_rows
+ * consecutive rows (the diagonal blocks of a batched block-diagonal matrix,
+ * e.g. one block per attention head); seg_rows ≤ 0 means a single run.
+ *
+ *   row_offsets : int32[M+1] (only lengths are read).
+ *   swizzle_out : int32[M], written with the permutation.
+ *   workspace   : at least row_swizzle_workspace_bytes(M, K) bytes of device
+ *                 scratch (contents ignored on entry).
+ * Bit-exact and deterministic.  M = 0 is a no-op.
+ */
+size_t row_swizzle_workspace_bytes(int M, int K);
+
+int row_swizzle_build(int M, int K, int seg_rows, const int *row_offsets, int *swizzle_out,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * usm_poll_status — synchronise `stream`, then return and clear the current
+ * device's status word: USM_OK, or USM_ERR_TIMEOUT when a kernel's bounded
+ * wait (on a TMA transfer) gave up and the kernel returned early (its output
+ * is then incomplete).  Returns USM_ERR_CUDA if the synchronisation fails.
+ */
+int usm_poll_status(void *stream);
+
+/* Human-readable name of a usm_status value (static string, never NULL). */
+const char *usm_status_string(int status);
+
+/*
+ * usm_selftest_wait_timeout — checks the bounded-wait path without faulting
+ * anything: launches one CTA that waits on a shared-memory barrier nothing
+ * will ever complete, with a limit of `limit_ns` nanoseconds (1e3..1e9).
+ * The kernel gives up, records USM_ERR_TIMEOUT in the status word and
+ * returns, so the next usm_poll_status(stream) returns USM_ERR_TIMEOUT.
+ */
+int usm_selftest_wait_timeout(long long limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USM_H_ */

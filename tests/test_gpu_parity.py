@@ -1,0 +1,356 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Small cases are compared in full (several tiles, ragged tails, edge cases);
+the five workload configurations at full size are compared on sampled rows
+the oracle computes one by one, in the same launch configuration the
+benchmark times.  Swizzles are compared bit-exactly; integer-valued inputs
+must match bit-exactly too (every partial sum is an exact integer)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from parity_util import TOL, assert_within, dev, host, oracle_sddmm, oracle_spmm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def csr_dev(csr):
+    return dev(csr.row_offsets), dev(csr.col_indices), dev(csr.values, csr.dtype)
+
+
+# ---------------------------------------------------------------------------
+# Row swizzle (bit-exact)
+# ---------------------------------------------------------------------------
+SWIZZLE_CASES = [
+    ("tiny", lambda: W.tiny().csr, 0),
+    ("ragged", lambda: W.random_csr(1, 5000, 300, 0.1), 0),
+    ("ragged_seg", lambda: W.random_csr(2, 5000, 300, 0.1), 1000),
+    ("one_row", lambda: W.random_csr(3, 1, 10, 0.5), 0),
+    ("all_empty", lambda: W.random_csr(4, 300, 10, 0.0), 0),
+    ("equal_lengths", lambda: W.random_csr(5, 777, 64, 0.0, lengths=np.full(777, 5)), 0),
+    ("long_tail", lambda: W.random_csr(6, 3000, 70000, 0.0, lengths=np.r_[np.zeros(2999, int), [65000]]), 0),
+    ("multi_tile_seg", lambda: W.random_csr(7, 9000, 100, 0.2), 4096),
+]
+
+
+@pytest.mark.parametrize("name,make,seg", SWIZZLE_CASES, ids=[c[0] for c in SWIZZLE_CASES])
+def test_swizzle_bit_exact(usm, name, make, seg):
+    csr = make()
+    got = host(usm.row_swizzle(dev(csr.row_offsets), csr.K, seg))
+    assert np.array_equal(got, oracle.row_swizzle(csr.row_offsets, seg))
+
+
+def test_swizzle_full_configs(usm):
+    for csr, seg in [(W.resnet(with_sddmm=False).csr, 0), (W.lstm(90).csr, 0),
+                     (W.ffn(4096, 1024, 90, with_spmm=False, with_sddmm=False).csr, 0),
+                     (W.attention().csr, 4096)]:
+        got = host(usm.row_swizzle(dev(csr.row_offsets), csr.K, seg))
+        assert np.array_equal(got, oracle.row_swizzle(csr.row_offsets, seg))
+
+
+# ---------------------------------------------------------------------------
+# SpMM, small and ragged, compared in full
+# ---------------------------------------------------------------------------
+SPMM_SHAPES = [
+    (1, 1, 1, 1.0), (5, 7, 3, 0.5), (37, 61, 64, 0.3), (130, 300, 129, 0.2), (257, 1000, 200, 0.1),
+    (300, 129, 513, 0.05), (64, 4097, 128, 0.3), (1000, 50, 8, 0.9), (513, 2000, 4, 0.02),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,K,N,density", SPMM_SHAPES)
+@pytest.mark.parametrize("swz", [False, True])
+def test_spmm_small(usm, dtype, M, K, N, density, swz):
+    csr = W.random_csr([M, K, N, 31], M, K, density, dtype=dtype)
+    B = W.dense(np.random.default_rng([M, K, N, 32]), K, N, 1.0, dtype)
+    ro, ci, vals = csr_dev(csr)
+    perm = usm.row_swizzle(ro, K) if swz else None
+    C = host(usm.spmm(ro, ci, vals, dev(B, dtype), K=K, row_swizzle=perm))
+    ref, S = oracle_spmm(csr, B, dtype)
+    assert_within(C, ref, S, TOL[dtype], f"spmm {dtype} {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_spmm_row_length_mix(usm, dtype):
+    # Every row length 0..9, then some long rows, every start residue.
+    lengths = np.r_[np.arange(10).repeat(7), [500, 1999, 2000, 33, 64, 65, 127, 128, 129]]
+    rng = np.random.default_rng(40)
+    lengths = rng.permutation(lengths)
+    M, K, N = lengths.size, 2000, 136
+    csr = W.random_csr(41, M, K, 0.0, dtype=dtype, lengths=lengths)
+    B = W.dense(np.random.default_rng(42), K, N, 1.0, dtype)
+    ro, ci, vals = csr_dev(csr)
+    C = host(usm.spmm(ro, ci, vals, dev(B, dtype), K=K, row_swizzle=usm.row_swizzle(ro, K)))
+    ref, S = oracle_spmm(csr, B, dtype)
+    assert_within(C, ref, S, TOL[dtype], "row length mix")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [64, 128, 300])
+def test_spmm_integer_valued_bit_exact(usm, dtype, N):
+    M, K = 300, 700
+    csr = W.random_csr([M, K, 43], M, K, 0.2, dtype=dtype, int_valued=True)
+    B = W.dense(np.random.default_rng(44), K, N, 1.0, dtype, int_valued=True)
+    ro, ci, vals = csr_dev(csr)
+    C = host(usm.spmm(ro, ci, vals, dev(B, dtype), K=K))
+    ref, _ = oracle_spmm(csr, B, dtype)
+    assert np.array_equal(C.astype(np.float64), ref)
+
+
+def test_spmm_identity_and_permutation_bit_exact(usm):
+    n, N = 1000, 72
+    B = W.dense(np.random.default_rng(45), n, N)
+    perm = np.random.default_rng(46).permutation(n).astype(np.int32)
+    ro = np.arange(n + 1, dtype=np.int32)
+    ones = np.ones(n, dtype=np.float32)
+    for cols in (np.arange(n, dtype=np.int32), perm):
+        C = host(usm.spmm(dev(ro), dev(cols), dev(ones), dev(B), K=n))
+        assert np.array_equal(C, B[cols])
+
+
+def test_spmm_empty_cases(usm):
+    import torch
+    # nnz = 0: C is zero-filled (the buffer starts as garbage)
+    csr = W.random_csr(47, 50, 40, 0.0)
+    B = W.dense(np.random.default_rng(48), 40, 24)
+    out = torch.full((50, 24), float("nan"), device="cuda")
+    ro, ci, vals = csr_dev(csr)
+    C = host(usm.spmm(ro, ci, vals, dev(B), K=40, out=out))
+    assert np.array_equal(C, np.zeros((50, 24), np.float32))
+    # M = 0 and N = 0 are no-ops
+    z = usm.spmm(dev(np.zeros(1, np.int32)), ci, vals, dev(B), K=40)
+    assert z.shape == (0, 24)
+    # rows that are all empty but one
+    lengths = np.zeros(300, int)
+    lengths[123] = 40
+    csr = W.random_csr(49, 300, 40, 0.0, lengths=lengths)
+    ro, ci, vals = csr_dev(csr)
+    C = host(usm.spmm(ro, ci, vals, dev(B), K=40))
+    ref, S = oracle_spmm(csr, B, "f32")
+    assert_within(C, ref, S, TOL["f32"], "one nonempty row")
+
+
+def test_spmm_leading_dimensions(usm):
+    import torch
+    M, K, N = 200, 300, 100
+    csr = W.random_csr(50, M, K, 0.1)
+    Bbig = W.dense(np.random.default_rng(51), K, 132)
+    Bv = dev(Bbig)[:, :N]
+    out = torch.zeros((M, 104), device="cuda")
+    ro, ci, vals = csr_dev(csr)
+    usm.spmm(ro, ci, vals, Bv, K=K, out=out[:, :N])
+    ref, S = oracle_spmm(csr, np.ascontiguousarray(Bbig[:, :N]), "f32")
+    C = host(out)
+    assert_within(C[:, :N], ref, S, TOL["f32"], "ld")
+    assert np.all(C[:, N:] == 0), "wrote outside the N columns"
+
+
+def test_spmm_swizzle_does_not_change_bits(usm):
+    csr = W.random_csr(52, 3000, 800, 0.15)
+    B = W.dense(np.random.default_rng(53), 800, 256)
+    ro, ci, vals = csr_dev(csr)
+    Bd = dev(B)
+    a = host(usm.spmm(ro, ci, vals, Bd, K=800))
+    b = host(usm.spmm(ro, ci, vals, Bd, K=800, row_swizzle=usm.row_swizzle(ro, 800)))
+    c = host(usm.spmm(ro, ci, vals, Bd, K=800))
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+# ---------------------------------------------------------------------------
+# SDDMM, small and ragged, compared in full
+# ---------------------------------------------------------------------------
+SDDMM_SHAPES = [
+    (1, 1, 1, 1.0), (7, 5, 3, 0.6), (37, 61, 64, 0.3), (130, 300, 129, 0.2), (257, 1000, 200, 0.1),
+    (300, 129, 513, 0.05), (64, 2100, 128, 0.3), (1000, 50, 8, 0.9), (40, 70, 1000, 0.2),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,K,D,density", SDDMM_SHAPES)
+@pytest.mark.parametrize("swz", [False, True])
+def test_sddmm_small(usm, dtype, M, K, D, density, swz):
+    csr = W.random_csr([M, K, D, 61], M, K, density, dtype=dtype)
+    rng = np.random.default_rng([M, K, D, 62])
+    X = W.dense(rng, M, D, 1.0, dtype)
+    Y = W.dense(rng, K, D, 1.0, dtype)
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    perm = usm.row_swizzle(ro, K) if swz else None
+    out = host(usm.sddmm(ro, ci, dev(X, dtype), dev(Y, dtype), row_swizzle=perm))
+    ref, S, _ = oracle_sddmm(csr, X, Y, dtype)
+    assert_within(out, ref, S, TOL[dtype], f"sddmm {dtype} {M}x{K}x{D}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("D", [64, 128, 300])
+def test_sddmm_integer_valued_bit_exact(usm, dtype, D):
+    M, K = 300, 700
+    csr = W.random_csr([M, K, 63], M, K, 0.2, dtype=dtype, int_valued=True)
+    rng = np.random.default_rng(64)
+    X = W.dense(rng, M, D, 1.0, dtype, int_valued=True)
+    Y = W.dense(rng, K, D, 1.0, dtype, int_valued=True)
+    out = host(usm.sddmm(dev(csr.row_offsets), dev(csr.col_indices), dev(X, dtype), dev(Y, dtype)))
+    ref, _, _ = oracle_sddmm(csr, X, Y, dtype)
+    assert np.array_equal(out.astype(np.float64), ref)
+
+
+def test_sddmm_bf16_output_rounding(usm):
+    import torch
+    M, K, D = 200, 300, 96
+    csr = W.random_csr(65, M, K, 0.2)
+    rng = np.random.default_rng(66)
+    X, Y = W.dense(rng, M, D), W.dense(rng, K, D)
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    f32 = usm.sddmm(ro, ci, dev(X), dev(Y))
+    b16 = host(usm.sddmm(ro, ci, dev(X), dev(Y), out_dtype=torch.bfloat16))
+    # The bf16 output is the fp32 result rounded to nearest even.
+    want = f32.to(torch.bfloat16).view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(b16, want)
+
+
+def test_sddmm_row_length_mix_and_empty(usm):
+    lengths = np.r_[np.arange(10).repeat(5), [0] * 20, [700, 1500, 32, 33, 31]]
+    lengths = np.random.default_rng(67).permutation(lengths)
+    M, K, D = lengths.size, 1500, 200
+    csr = W.random_csr(68, M, K, 0.0, lengths=lengths)
+    rng = np.random.default_rng(69)
+    X, Y = W.dense(rng, M, D), W.dense(rng, K, D)
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    out = host(usm.sddmm(ro, ci, dev(X), dev(Y), row_swizzle=usm.row_swizzle(ro, K)))
+    ref, S, _ = oracle_sddmm(csr, X, Y, "f32")
+    assert_within(out, ref, S, TOL["f32"], "sddmm length mix")
+
+
+def test_sddmm_adjoint_identity_on_gpu(usm):
+    # sum(SpMM(S,B) ⊙ C) = sum(vals ⊙ SDDMM_S(C, B)), both sides from the GPU.
+    M, K, N = 500, 400, 96
+    csr = W.random_csr(70, M, K, 0.1)
+    rng = np.random.default_rng(71)
+    B, Cm = W.dense(rng, K, N), W.dense(rng, M, N)
+    ro, ci, vals = csr_dev(csr)
+    lhs = np.sum(host(usm.spmm(ro, ci, vals, dev(B), K=K)).astype(np.float64) * Cm)
+    rhs = np.sum(csr.values.astype(np.float64) * host(usm.sddmm(ro, ci, dev(Cm), dev(B))))
+    scale = np.sum(np.abs(csr.values)) * np.abs(B).max() * np.abs(Cm).max() * 4
+    assert abs(lhs - rhs) <= 1e-5 * scale
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, sampled rows (same launch configuration as bench.py)
+# ---------------------------------------------------------------------------
+def _spmm_full(usm, p, seed, nrows=192):
+    csr = p.csr
+    ro, ci, vals = csr_dev(csr)
+    perm = usm.row_swizzle(ro, csr.K)
+    C = host(usm.spmm(ro, ci, vals, dev(p.B, p.dtype), K=csr.K, row_swizzle=perm))
+    rows = sample_rows(csr.M, nrows, seed, host(perm))
+    ref, S = oracle_spmm(csr, p.B, p.dtype, rows)
+    assert_within(C[rows], ref, S, TOL[p.dtype], p.name + " spmm")
+
+
+def _sddmm_full(usm, p, seed, nrows=192):
+    csr = p.csr
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    perm = usm.row_swizzle(ro, csr.K)
+    out = host(usm.sddmm(ro, ci, dev(p.X, p.dtype), dev(p.Y, p.dtype), row_swizzle=perm))
+    rows = sample_rows(csr.M, nrows, seed, host(perm))
+    ref, S, pos = oracle_sddmm(csr, p.X, p.Y, p.dtype, rows)
+    assert_within(out[pos], ref, S, TOL[p.dtype], p.name + " sddmm")
+
+
+@pytest.mark.slow
+def test_tiny_config_full(usm):
+    p = W.tiny()
+    csr = p.csr
+    ro, ci, vals = csr_dev(csr)
+    perm = usm.row_swizzle(ro, csr.K)
+    C = host(usm.spmm(ro, ci, vals, dev(p.B), K=csr.K, row_swizzle=perm))
+    ref, S = oracle_spmm(csr, p.B, "f32")
+    assert_within(C, ref, S, TOL["f32"], "tiny spmm")
+    out = host(usm.sddmm(ro, ci, dev(p.X), dev(p.Y), row_swizzle=perm))
+    ref, S, _ = oracle_sddmm(csr, p.X, p.Y, "f32")
+    assert_within(out, ref, S, TOL["f32"], "tiny sddmm")
+
+
+@pytest.mark.slow
+def test_resnet_config(usm):
+    p = W.resnet()
+    _spmm_full(usm, p, 80)
+    _sddmm_full(usm, p, 81)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", W.FFN_SHAPES, ids=["4096x1024", "1024x4096"])
+@pytest.mark.parametrize("s", W.FFN_SPARSITIES)
+def test_ffn_config(usm, dtype, shape, s):
+    p = W.ffn(shape[0], shape[1], s, dtype)
+    _spmm_full(usm, p, 90 + s, nrows=96)
+    _sddmm_full(usm, p, 91 + s, nrows=96)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("s", W.LSTM_SPARSITIES)
+def test_lstm_config(usm, s):
+    _spmm_full(usm, W.lstm(s), 100 + s, nrows=96)
+
+
+@pytest.mark.slow
+def test_attention_chain(usm):
+    """SDDMM scores (fp32 accumulation, rounded to bf16), then SpMM of the
+    scores with V: the sparse-attention use of the two kernels."""
+    import torch
+    p = W.attention()
+    csr = p.csr
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    perm = usm.row_swizzle(ro, csr.K, seg_rows=p.meta["seq"])
+    Q, Kt, V = dev(p.X, "bf16"), dev(p.Y, "bf16"), dev(p.V, "bf16")
+    s32 = usm.sddmm(ro, ci, Q, Kt, row_swizzle=perm)
+    s16 = usm.sddmm(ro, ci, Q, Kt, row_swizzle=perm, out_dtype=torch.bfloat16)
+    O = host(usm.spmm(ro, ci, s16, V, K=csr.K, row_swizzle=perm))
+    rows = sample_rows(csr.M, 128, 110, host(perm))
+    # scores
+    ref_s, S_s, pos = oracle_sddmm(csr, p.X, p.Y, "bf16", rows)
+    assert_within(host(s32)[pos], ref_s, S_s, TOL["bf16"], "attention scores")
+    # rounded scores: bf16 of the fp32 sums; equal to the oracle's rounding
+    # except where the fp32 sum and the exact sum straddle a rounding tie
+    got16 = host(s16)[pos]
+    want16 = oracle.round_to_bf16(ref_s)
+    diff = np.abs(got16.astype(np.int64) - want16.astype(np.int64))
+    assert np.all(diff <= 1) and np.mean(diff == 0) > 0.99
+    # chain output against the oracle chain, with the oracle's own rounding
+    sub_ro, sub_ci, _ = oracle.select_rows(csr.row_offsets, csr.col_indices, rows)
+    vals64 = oracle.widen(want16, "bf16")
+    Vw = oracle.widen(p.V, "bf16")
+    ref_o = oracle.spmm(rows.size, csr.K, sub_ro, sub_ci, vals64, Vw)
+    S_o = oracle.spmm_error_scale(rows.size, csr.K, sub_ro, sub_ci, vals64, Vw)
+    assert_within(O[rows], ref_o, S_o, TOL["bf16"], "attention output")
+
+
+# ---------------------------------------------------------------------------
+# Status word and bounded waits
+# ---------------------------------------------------------------------------
+def test_bounded_wait_times_out_cleanly(usm):
+    import torch
+    lib = usm.load()
+    assert usm.poll_status() == 0
+    assert lib.usm_selftest_wait_timeout(2_000_000, usm._stream()) == 0   # 2 ms
+    assert usm.poll_status() == -5
+    assert usm.poll_status() == 0   # read-and-clear
+    # the context is still usable
+    x = torch.ones(10, device="cuda")
+    assert float(x.sum()) == 10.0
+
+
+def test_misaligned_pointer_rejected(usm):
+    import torch
+    csr = W.random_csr(120, 10, 10, 0.3)
+    ro, ci, vals = csr_dev(csr)
+    B = torch.zeros((10, 9), device="cuda")[:, 1:]   # offset by 4 bytes, ld 9
+    C = torch.zeros((10, 8), device="cuda")
+    lib = usm.load()
+    code = lib.csr_spmm(10, 10, 8, csr.nnz, ro.data_ptr(), ci.data_ptr(), vals.data_ptr(), None,
+                        B.data_ptr(), 9, C.data_ptr(), 8, 0, usm._stream())
+    assert code == -2
+    # the binding pads such operands itself and gets the right answer
+    Cb = host(usm.spmm(ro, ci, vals, B, K=10))
+    assert np.array_equal(Cb, np.zeros((10, 8), np.float32))

@@ -1,0 +1,64 @@
+// Host-side declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "usm.h"
+
+namespace usm {
+
+struct SpmmArgs {
+    int M, K, N, nnz;
+    const int* row_offsets;
+    const int* col_indices;
+    const void* values;
+    const int* perm;  // may be null (identity order)
+    float* C;
+    long long ldc;
+    int* status;
+};
+
+struct SddmmArgs {
+    int M, K, D, nnz;
+    const int* row_offsets;
+    const int* col_indices;
+    const int* perm;
+    const void* X;
+    long long ldx;
+    void* out;           // final output (single strip) or fp32 partials (several strips)
+    long long out_stride;  // elements between strips of partials
+    int out_bf16;        // final output element type is bf16
+    int rows_per_warp;
+    int* status;
+};
+
+// Device status word of the current device (null if it cannot be resolved).
+int* status_word_for_current_device();
+
+// Number of SMs of the current device (cached per device).
+int sm_count_current_device();
+
+// Encode a 2-D row-major tensor map (inner dim = cols) with box
+// {box_cols, box_rows}.  Returns false if the driver entry point is missing
+// or the encode fails.
+bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool bf16, long long rows,
+                          long long cols, long long ld_elems, int box_cols, int box_rows);
+
+int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream);
+int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream);
+
+size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16);
+int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream);
+
+size_t swizzle_workspace_bytes(int M, int K);
+int launch_row_swizzle(int M, int K, int seg_rows, const int* row_offsets, int* perm,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+int launch_wait_timeout_selftest(long long limit_ns, int* status, cudaStream_t stream);
+
+}  // namespace usm

@@ -1,0 +1,417 @@
+// CSR SDDMM for sm_103a: out[p] = X[r]·Y[col_p] on the nonzeros of the mask.
+//
+// "Sparse GPU Kernels for Deep Learning" (Gale et al., SC 2020), summary
+// card, "Interesting ideas" I3: the kernel drops the element-wise scaling by
+// the mask's values and takes the second operand transposed (Y is K×D and
+// the product is X·Yᵀ), the form weight gradients and sparse-attention
+// scores need.  GB300 design:
+//
+// * Tiles.  A CTA owns MT = R·W mask rows (row-swizzle order, R chosen at
+//   launch) and one strip of DT columns of D.  It walks K in chunks of KC
+//   rows; one thread copies Y[k0:k0+KC, d0:d0+DT] into a shared-memory stage
+//   with TMA (double buffered, mbarrier, bounded wait).
+// * Per (row, chunk) a warp keeps X[r, d0:d0+DT] in registers (fp32), reads
+//   the row's next 32 column indices (coalesced window after its cursor),
+//   keeps the prefix inside the chunk and lists their stage offsets.
+// * Dot products.  Lanes form G = 32/L groups of L lanes; at step t group g
+//   takes list entry t·G+g and each lane multiplies its VV·EPV elements of
+//   the staged Y row with its X elements (f32x2 FMA), leaving one partial per
+//   step.  After L steps the L partials of each lane are reduced across the L
+//   lanes of the group with a transpose-reduction (L-1 shuffles for L
+//   results), so lane l of group g ends up with entry l·G+g's strip sum.
+// * Strips.  With one strip the result goes straight to `out` (fp32 or bf16
+//   rounded to nearest even).  With several, each strip writes fp32 partials
+//   to the caller's workspace and a second kernel adds the strips in order:
+//   no atomics, results are bit-reproducible.
+#include <climits>
+
+#include "usm_device.cuh"
+#include "usm_internal.h"
+
+namespace usm {
+namespace {
+
+template <bool BF, int L, int VV, int W, int KC>
+struct SddmmCfg {
+    static constexpr int EPV = BF ? 8 : 4;
+    static constexpr int DT = L * VV * EPV;     // D columns per CTA
+    static constexpr int G = 32 / L;
+    static constexpr int PITCH = L * VV * 16;   // bytes per staged Y row
+    static constexpr int STAGE = KC * PITCH;
+    static constexpr int BOX_ROWS = KC < 256 ? KC : 256;
+    static constexpr int THREADS = W * 32;
+    static constexpr int SMEM = 2 * STAGE + 64 + W * 32 * 4;
+    static_assert(G * L == 32, "groups must tile the warp");
+    static_assert(KC % BOX_ROWS == 0, "KC must be a multiple of the TMA box height");
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ int window_col(const SddmmArgs& a, int pos, int end, int lane) {
+    const int p = pos + lane;
+    return p < end ? __ldg(a.col_indices + p) : INT_MAX;
+}
+
+// X[r, d0 + j*L*EPV + l*EPV : +EPV] for j < VV as raw 32-bit words; zero
+// beyond D.
+template <bool BF, int L, int VV>
+__device__ __forceinline__ void load_x(const SddmmArgs& a, int row, int d0, int l,
+                                       uint32_t (&xw)[VV * (BF ? 4 : 4)]) {
+    constexpr int EPV = BF ? 8 : 4;
+#pragma unroll
+    for (int j = 0; j < VV; ++j) {
+        const int c = d0 + j * L * EPV + l * EPV;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row >= 0) {
+            if (BF) {
+                const unsigned short* x =
+                    reinterpret_cast<const unsigned short*>(a.X) + (long long)row * a.ldx + c;
+                if (c + EPV <= a.D) {
+                    v = __ldg(reinterpret_cast<const uint4*>(x));
+                } else {
+                    uint32_t h[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) h[e] = (c + e < a.D) ? __ldg(x + e) : 0u;
+                    v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                   h[6] | (h[7] << 16));
+                }
+            } else {
+                const float* x = reinterpret_cast<const float*>(a.X) + (long long)row * a.ldx + c;
+                if (c + EPV <= a.D) {
+                    v = __ldg(reinterpret_cast<const uint4*>(x));
+                } else {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        h[e] = (c + e < a.D) ? __float_as_uint(__ldg(x + e)) : 0u;
+                    v = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+            }
+        }
+        xw[4 * j + 0] = v.x;
+        xw[4 * j + 1] = v.y;
+        xw[4 * j + 2] = v.z;
+        xw[4 * j + 3] = v.w;
+    }
+}
+
+template <bool BF, int L, int VV, int W, int KC>
+__global__ void __launch_bounds__(W * 32, 1)
+    sddmm_kernel(const __grid_constant__ CUtensorMap tmY, const SddmmArgs a) {
+    using C_ = SddmmCfg<BF, L, VV, W, KC>;
+    constexpr int EPV = C_::EPV, G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE;
+    constexpr int NX = VV * EPV;  // X elements per lane
+
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* stages = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * STAGE);
+    int* kr = reinterpret_cast<int*>(smem + 2 * STAGE + 16);
+    uint32_t* lists = reinterpret_cast<uint32_t*>(smem + 2 * STAGE + 64);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / L, l = lane % L;
+    const int R = a.rows_per_warp;  // ≤ 32
+    const int MT = R * W;
+    const int tile = blockIdx.x;
+    const int strip = blockIdx.y;
+    const int d0 = strip * C_::DT;
+
+    if (threadIdx.x == 0) {
+        kr[0] = INT_MAX;
+        kr[1] = -1;
+        kr[2] = 0;
+        mbar_init(smem_addr(&bars[0]), 1);
+        mbar_init(smem_addr(&bars[1]), 1);
+        fence_barrier_init();
+        prefetch_tensor_map(&tmY);
+    }
+
+    int my_row = -1, my_start = 0, my_end = 0;
+    if (lane < R) {
+        const long long m = (long long)tile * MT + (long long)lane * W + warp;
+        if (m < a.M) {
+            const int r = a.perm ? __ldg(a.perm + m) : (int)m;
+            if ((unsigned)r < (unsigned)a.M) {
+                int s = __ldg(a.row_offsets + r), e = __ldg(a.row_offsets + r + 1);
+                s = min(max(s, 0), a.nnz);
+                e = min(max(e, s), a.nnz);
+                my_row = r;
+                my_start = s;
+                my_end = e;
+            }
+        }
+    }
+    int kmin = INT_MAX, kmax = -1;
+    if (my_end > my_start) {
+        kmin = __ldg(a.col_indices + my_start);
+        kmax = __ldg(a.col_indices + my_end - 1);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(kFullMask, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(kFullMask, kmax, o));
+    }
+    __syncthreads();
+    if (lane == 0 && kmax >= 0) {
+        atomicMin(&kr[0], kmin);
+        atomicMax(&kr[1], kmax);
+    }
+    __syncthreads();
+    int c_lo = 0, nchunks = 0;
+    {
+        const int lo = max(kr[0], 0), hi = min(kr[1], a.K - 1);
+        if (kr[1] >= 0 && lo <= hi) {
+            c_lo = lo / KC;
+            nchunks = hi / KC - c_lo + 1;
+        }
+    }
+
+    auto issue = [&](int j) {
+        const int s = j & 1;
+        const uint32_t bar = smem_addr(&bars[s]);
+        mbar_arrive_expect_tx(bar, STAGE);
+        const uint32_t dst = smem_addr(stages + s * STAGE);
+#pragma unroll
+        for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
+            tma_load_2d(dst + b * C_::BOX_ROWS * PITCH, &tmY, d0, (c_lo + j) * KC + b * C_::BOX_ROWS,
+                        bar);
+    };
+    if (threadIdx.x == 0) {
+        if (nchunks > 0) issue(0);
+        if (nchunks > 1) issue(1);
+    }
+
+    int cur = my_start;
+    // Prefetched state of the next row to process: its window and X strip.
+    int pcol = window_col(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), lane);
+    uint32_t pxw[VV * 4];
+    load_x<BF, L, VV>(a, __shfl_sync(kFullMask, my_row, 0), d0, l, pxw);
+
+    uint32_t* wl = lists + warp * 32;
+    const bool single_strip = gridDim.y == 1;
+
+    for (int j = 0; j < nchunks; ++j) {
+        const int s = j & 1;
+        const int k0 = (c_lo + j) * KC;
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j >> 1) & 1, kWaitLimitNs);
+        if (!ok) kr[2] = 1;
+        const uint32_t stage = smem_addr(stages + s * STAGE) + l * 16;
+        if (ok) {
+#pragma unroll 1
+            for (int i = 0; i < R; ++i) {
+                int rc = __shfl_sync(kFullMask, cur, i);
+                const int re = __shfl_sync(kFullMask, my_end, i);
+                int col = pcol;
+                float x[NX];
+                if (BF) {
+#pragma unroll
+                    for (int q = 0; q < NX / 2; ++q) {
+                        x[2 * q] = bf16lo(pxw[q]);
+                        x[2 * q + 1] = bf16hi(pxw[q]);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < NX; ++q) x[q] = __uint_as_float(pxw[q]);
+                }
+                // Prefetch the next row slot (or slot 0 for the next chunk; its
+                // cursor is final once slot 0 has been processed, which holds
+                // when R > 1; for R == 1 the reload below after the segment
+                // covers it).
+                {
+                    const int ni = (i + 1 < R) ? i + 1 : 0;
+                    if (ni != i) {
+                        pcol = window_col(a, __shfl_sync(kFullMask, cur, ni),
+                                          __shfl_sync(kFullMask, my_end, ni), lane);
+                        load_x<BF, L, VV>(a, __shfl_sync(kFullMask, my_row, ni), d0, l, pxw);
+                    }
+                }
+                while (true) {
+                    const bool valid = (rc + lane < re) && ((unsigned)(col - k0) < (unsigned)KC);
+                    const unsigned bal = __ballot_sync(kFullMask, valid);
+                    const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);
+                    if (n == 0) break;
+                    wl[lane] = (lane < n) ? (uint32_t)(col - k0) * PITCH : 0u;
+                    __syncwarp();
+                    float part[L];
+#pragma unroll
+                    for (int t = 0; t < L; ++t) {
+                        part[t] = 0.f;
+                        if (t * G < n) {
+                            const uint32_t off = wl[t * G + g];
+                            float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int jj = 0; jj < VV; ++jj) {
+                                const uint4 y = lds128(stage + off + jj * L * 16);
+                                if (BF) {
+                                    const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q)
+                                        s2 = __ffma2_rn(make_float2(x[jj * 8 + 2 * q], x[jj * 8 + 2 * q + 1]),
+                                                        make_float2(bf16lo(w[q]), bf16hi(w[q])), s2);
+                                } else {
+                                    s2 = __ffma2_rn(make_float2(x[jj * 4], x[jj * 4 + 1]),
+                                                    make_float2(__uint_as_float(y.x), __uint_as_float(y.y)), s2);
+                                    s2 = __ffma2_rn(make_float2(x[jj * 4 + 2], x[jj * 4 + 3]),
+                                                    make_float2(__uint_as_float(y.z), __uint_as_float(y.w)), s2);
+                                }
+                            }
+                            part[t] = s2.x + s2.y;
+                        }
+                    }
+                    // Transpose-reduce across the L lanes of each group: after it,
+                    // lane l holds the group's sum for step l.
+#pragma unroll
+                    for (int off = L / 2; off >= 1; off >>= 1) {
+                        const bool upper = (l & off) != 0;
+#pragma unroll
+                        for (int q = 0; q < off; ++q) {
+                            const float send = upper ? part[q] : part[q + off];
+                            const float keep = upper ? part[q + off] : part[q];
+                            part[q] = keep + __shfl_xor_sync(kFullMask, send, off);
+                        }
+                    }
+                    const int e = l * G + g;  // list entry whose sum this lane holds
+                    if (e < n) {
+                        const long long p = (long long)rc + e;
+                        if (single_strip) {
+                            if (a.out_bf16)
+                                reinterpret_cast<uint16_t*>(a.out)[p] = f32_to_bf16_rne(part[0]);
+                            else
+                                reinterpret_cast<float*>(a.out)[p] = part[0];
+                        } else {
+                            reinterpret_cast<float*>(a.out)[(long long)strip * a.out_stride + p] = part[0];
+                        }
+                    }
+                    __syncwarp();
+                    rc += n;
+                    if (n < 32) break;
+                    col = window_col(a, rc, re, lane);
+                }
+                if (lane == i) cur = rc;
+                if (R == 1) {
+                    pcol = window_col(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0),
+                                      lane);
+                }
+            }
+        }
+        __syncthreads();
+        if (kr[2]) break;
+        if (threadIdx.x == 0 && j + 2 < nchunks) {
+            fence_proxy_async_smem();
+            issue(j + 2);
+        }
+    }
+
+    if (kr[2] && threadIdx.x == 0) {
+        record_status(a.status, USM_ERR_TIMEOUT);
+        for (int b = 0; b < 2 && b < nchunks; ++b) {
+            mbar_wait_bounded(smem_addr(&bars[b]), 0, 1000000ull);
+            mbar_wait_bounded(smem_addr(&bars[b]), 1, 1000000ull);
+        }
+    }
+}
+
+// out[p] = Σ_s partial[s][p], strips added in increasing order.
+__global__ void sddmm_strip_sum_kernel(const float* __restrict__ part, long long nnz, int nstrips,
+                                       void* out, int out_bf16) {
+    for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < nnz;
+         p += (long long)gridDim.x * blockDim.x) {
+        float s = part[p];
+        for (int k = 1; k < nstrips; ++k) s += part[(long long)k * nnz + p];
+        if (out_bf16)
+            reinterpret_cast<uint16_t*>(out)[p] = f32_to_bf16_rne(s);
+        else
+            reinterpret_cast<float*>(out)[p] = s;
+    }
+}
+
+__global__ void fill_out_kernel(void* out, long long n, int bf16) {
+    for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n;
+         p += (long long)gridDim.x * blockDim.x) {
+        if (bf16)
+            reinterpret_cast<uint16_t*>(out)[p] = 0;
+        else
+            reinterpret_cast<float*>(out)[p] = 0.f;
+    }
+}
+
+template <bool BF, int L, int VV, int W, int KC>
+int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    using C_ = SddmmCfg<BF, L, VV, W, KC>;
+    CUtensorMap map;
+    if (!encode_tensor_map_2d(&map, Y, BF, a.K, a.D, ldy, C_::DT, C_::BOX_ROWS)) return USM_ERR_CUDA;
+    auto kern = sddmm_kernel<BF, L, VV, W, KC>;
+    static int configured_mask = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM) !=
+            cudaSuccess)
+            return USM_ERR_CUDA;
+        __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
+    }
+    const int nstrips = (a.D + C_::DT - 1) / C_::DT;
+    if (nstrips > 65535) return USM_ERR_UNSUPPORTED;
+    void* final_out = a.out;
+    if (nstrips > 1) {
+        if (ws == nullptr || ws_bytes < (size_t)nstrips * (size_t)a.nnz * sizeof(float))
+            return USM_ERR_WORKSPACE;
+        a.out = ws;
+        a.out_stride = a.nnz;
+    }
+    // Rows per warp: as many as keep ≥ 2 CTAs per SM in flight (up to 32).
+    const int sms = sm_count_current_device();
+    int R = 32;
+    while (R > 1 && (long long)((a.M + R * W - 1) / (R * W)) * nstrips < 2LL * sms) R >>= 1;
+    a.rows_per_warp = R;
+    const dim3 grid((a.M + R * W - 1) / (R * W), nstrips);
+    kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);
+    if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
+    if (nstrips > 1) {
+        long long blocks = ((long long)a.nnz + 255) / 256;
+        if (blocks > 8 * sms) blocks = 8 * sms;
+        sddmm_strip_sum_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz,
+                                                                nstrips, final_out, a.out_bf16);
+        if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
+    }
+    return USM_OK;
+}
+
+// Strip width by element type and D: fp32 strips are 128 wide (8 lanes x 16
+// values), bf16 strips 128 wide, or 64 when D ≤ 64.
+int strip_width(int D, bool bf16) { return (bf16 && D <= 64) ? 64 : 128; }
+
+}  // namespace
+
+size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16) {
+    (void)M;
+    (void)K;
+    if (D <= 0 || nnz <= 0) return 0;
+    const int dt = strip_width(D, bf16);
+    const long long nstrips = (D + dt - 1) / dt;
+    return nstrips > 1 ? (size_t)nstrips * (size_t)nnz * sizeof(float) : 0;
+}
+
+int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream) {
+    if (n <= 0) return USM_OK;
+    long long blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    fill_out_kernel<<<(int)blocks, 256, 0, stream>>>(out, n, bf16 ? 1 : 0);
+    return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
+}
+
+int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, size_t ws_bytes,
+                 cudaStream_t stream) {
+    constexpr int W = 16;
+    if (!in_bf16) return launch_cfg<false, 8, 4, W, 128>(a, Y, ldy, ws, ws_bytes, stream);
+    if (a.D <= 64) return launch_cfg<true, 8, 1, W, 512>(a, Y, ldy, ws, ws_bytes, stream);
+    return launch_cfg<true, 8, 2, W, 256>(a, Y, ldy, ws, ws_bytes, stream);
+}
+
+}  // namespace usm
