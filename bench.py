@@ -1,0 +1,464 @@
+"""Benchmark: CSR SpMM / SDDMM useful throughput on GB300.
+
+One step = one pass of the whole hot path over the Transformer-FFN workload
+of "Sparse GPU Kernels for Deep Learning" (Gale et al., SC 2020) as
+configured here: sparse weights A of 4096x1024 and 1024x4096 at 70/80/90/95%
+sparsity, each used by the SpMM forward (C = A·B, B K x 2048) and the SDDMM
+weight gradient (mask(A) ⊙ X·Yᵀ with X M x 2048, Y K x 2048), in fp32 and in
+bf16-in/fp32-accumulate: 32 launches of the library per step.  The row
+swizzles are built once per sparsity pattern before timing (set-up, like the
+pattern itself).
+
+Metric: useful GFLOP/s = Σ 2·nnz·N over the step's products ÷ time.
+Output: one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores instead (bounded row samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+N_FFN = 2048
+SMS = 152
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ = 2070.0
+# FP32 CUDA-core peak: 152 SMs x 128 FMA lanes x 2 flop x 2.07 GHz.
+FP32_PEAK_TFLOPS = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+WORKLOAD = ("transformer_ffn: A 4096x1024 and 1024x4096 at 70/80/90/95% sparsity (row lengths "
+            "N(mu, (0.1mu)^2), uniform columns, values N(0,0.02)); SpMM forward with B Kx2048 and "
+            "SDDMM weight-gradient with X Mx2048, Y Kx2048, N(0,1); fp32 and bf16-in/fp32-acc")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# Work list
+# ---------------------------------------------------------------------------
+def tag_of(dtype, M, K, s):
+    return f"{dtype}_{M}x{K}_s{s}"
+
+
+def problems(only=None):
+    """Problems of one step (each used by one SpMM and one SDDMM launch).
+    `only` keeps the problems whose tag contains that substring."""
+    out = []
+    for dtype in ("f32", "bf16"):
+        for (M, K) in W.FFN_SHAPES:
+            for s in W.FFN_SPARSITIES:
+                if only and only.split(":")[-1] not in tag_of(dtype, M, K, s):
+                    continue
+                out.append(W.ffn(M, K, s, dtype, N=N_FFN))
+    return out
+
+
+def ops_of(only):
+    """--only spmm:<tag> / sddmm:<tag> restricts the operation too."""
+    if only and ":" in only:
+        return (only.split(":")[0],)
+    return ("spmm", "sddmm")
+
+
+def flops_of(p, op):
+    return 2.0 * p.csr.nnz * N_FFN
+
+
+def alg_bytes(p, op):
+    """Bytes the operation must move at minimum (each operand once)."""
+    es = 2 if p.dtype == "bf16" else 4
+    M, K, nnz = p.csr.M, p.csr.K, p.csr.nnz
+    if op == "spmm":
+        return nnz * (es + 4) + 4 * (M + 1) + K * N_FFN * es + 4 * M * N_FFN
+    return nnz * (4 + 4) + 4 * (M + 1) + (M + K) * N_FFN * es
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import unstructured_sparse_matmul_gb300 as usm
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    usm.load()
+    stream = torch.cuda.current_stream()
+
+    def to_dev(x, dtype):
+        if dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    probs = problems(args.only)
+    if not probs:
+        raise SystemExit(f"--only {args.only!r} matches no launch")
+    items = []
+    for p in probs:
+        csr = p.csr
+        d = {
+            "p": p,
+            "ro": to_dev(csr.row_offsets, "i32"), "ci": to_dev(csr.col_indices, "i32"),
+            "vals": to_dev(csr.values, p.dtype),
+            "B": to_dev(p.B, p.dtype), "X": to_dev(p.X, p.dtype), "Y": to_dev(p.Y, p.dtype),
+        }
+        d["C"] = torch.empty((csr.M, N_FFN), dtype=torch.float32, device=dev)
+        d["out"] = torch.empty(csr.nnz, dtype=torch.float32, device=dev)
+        lib = usm.load()
+        ws_bytes = lib.csr_sddmm_workspace_bytes(csr.M, csr.K, N_FFN, csr.nnz, 1 if p.dtype == "bf16" else 0)
+        d["ws"] = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        d["perm"] = usm.row_swizzle(d["ro"], csr.K)
+        items.append(d)
+    torch.cuda.synchronize()
+
+    # Launch list of one step: (label, op, item)
+    launches = []
+    for d in items:
+        p = d["p"]
+        tag = tag_of(p.dtype, p.csr.M, p.csr.K, p.meta["sparsity"])
+        for op in ops_of(args.only):
+            launches.append((f"{op}_{tag}", op, d))
+    kernels_per_launch = {}
+    for label, op, d in launches:
+        p = d["p"]
+        n = 1
+        if op == "sddmm":
+            code = 1 if p.dtype == "bf16" else 0
+            n += 1 if lib.csr_sddmm_workspace_bytes(p.csr.M, p.csr.K, N_FFN, p.csr.nnz, code) > 0 else 0
+        kernels_per_launch[label] = n
+
+    def run_one(op, d):
+        if op == "spmm":
+            usm.spmm(d["ro"], d["ci"], d["vals"], d["B"], K=d["p"].csr.K, row_swizzle=d["perm"], out=d["C"])
+        else:
+            usm.sddmm(d["ro"], d["ci"], d["X"], d["Y"], row_swizzle=d["perm"], out=d["out"], workspace=d["ws"])
+
+    def step(events=None):
+        for i, (label, op, d) in enumerate(launches):
+            if events is not None:
+                events[i][0].record(stream)
+            run_one(op, d)
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if usm.poll_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    # Timed region: K steps, per-launch events on the launching stream.
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in launches]
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    if usm.poll_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+    per_launch_ms = {label: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
+                     for i, (label, _, _) in enumerate(launches)}
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    step_flops = sum(flops_of(d["p"], op) for _, op, d in launches)
+    step_bytes = sum(alg_bytes(d["p"], op) for _, op, d in launches)
+    value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+
+    # Dominant launch (largest time) and its roofline.
+    rows = []
+    for label, op, d in launches:
+        t = per_launch_ms[label] * 1e-3
+        fl, by = flops_of(d["p"], op), alg_bytes(d["p"], op)
+        rows.append({"launch": label, "ms": round(t * 1e3, 4), "tflops": round(fl / t / 1e12, 2),
+                     "alg_gbs": round(by / t / 1e9, 1),
+                     "frac_fp32": round(fl / t / 1e12 / FP32_PEAK_TFLOPS, 4)})
+    dom = max(rows, key=lambda r: r["ms"])
+    dom_label = dom["launch"]
+    traffic = recorded_traffic(dom_label)
+
+    # End to end through the public API with host buffers.
+    e2e = run_e2e(args, usm, torch, dev, launches, step_flops) if not args.no_e2e else None
+
+    result = {
+        "metric": "SpMM/SDDMM useful GFLOP/s (2·nnz·N), HBM GB/s, % of roofline on 1 GB300",
+        "value": round(value, 1),
+        "unit": "GFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded, shaped like the pages' Transformer-FFN weights)",
+        "config": {"workload": WORKLOAD if not args.only else f"{WORKLOAD} [only {args.only}]",
+                   "launches_per_step": len(launches),
+                   "l2": "inputs larger than L2: each step touches ~1.1 GB of operands",
+                   "swizzle": "row swizzle built once per pattern before timing",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hbm_alg_gbs": round(step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9, 1),
+        "roofline_frac_step": round(value / 1e3 / (FP32_PEAK_TFLOPS * world), 4),
+        "roofline": {"bound": "alu", "achieved": dom["tflops"], "peak": round(FP32_PEAK_TFLOPS, 2),
+                     "unit": "TFLOP/s", "frac": round(dom["tflops"] / FP32_PEAK_TFLOPS, 4),
+                     "traffic": traffic, "kernel": dom_label,
+                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"},
+        "per_launch": rows,
+        "gpu_launches": sum(kernels_per_launch[label] for label, _, _ in launches) * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_sample, args.only)
+    return result
+
+
+def recorded_traffic(label):
+    """DRAM bytes per launch from the committed ncu summary for this launch,
+    if it was captured on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.join(ROOT, "unstructured_sparse_matmul_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "unstructured_sparse_matmul_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    src = h.hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 3 and parts[0] == label and parts[2] == src:
+            return int(parts[1])
+    return None
+
+
+def run_e2e(args, usm, torch, dev, launches, step_flops):
+    """Same metric through the API with host buffers: every step copies the
+    step's inputs from pinned host memory and reads the results back."""
+    stream = torch.cuda.current_stream()
+    host_in, host_out = [], []
+    seen = set()
+    for label, op, d in launches:
+        key = id(d)
+        if key not in seen:
+            seen.add(key)
+            for name in ("ro", "ci", "vals", "B", "X", "Y"):
+                t = d[name]
+                host_in.append((t.cpu().pin_memory(), t))
+            d["perm_host"] = (d["perm"].cpu().pin_memory(), d["perm"])
+            host_in.append(d["perm_host"])
+        out_t = d["C"] if op == "spmm" else d["out"]
+        host_out.append((torch.empty(out_t.shape, dtype=out_t.dtype).pin_memory(), out_t))
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+    d2h = sum(h.numel() * h.element_size() for h, _ in host_out)
+
+    def e2e_step():
+        for h, dv in host_in:
+            dv.copy_(h, non_blocking=True)
+        for label, op, d in launches:
+            if op == "spmm":
+                usm.spmm(d["ro"], d["ci"], d["vals"], d["B"], K=d["p"].csr.K, row_swizzle=d["perm"], out=d["C"])
+            else:
+                usm.sddmm(d["ro"], d["ci"], d["X"], d["Y"], row_swizzle=d["perm"], out=d["out"], workspace=d["ws"])
+        for h, dv in host_out:
+            h.copy_(dv, non_blocking=True)
+
+    steps = max(2, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1)
+    return {"value": round(step_flops * steps / (ms * 1e-3) / 1e9, 1), "unit": "GFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (cpu_baseline / --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_sample_pass(probs, frac):
+    """Run the oracle on a row sample of every launch of one step; returns
+    (flops done, seconds)."""
+    import oracle
+    flops, secs = 0.0, 0.0
+    for p in probs:
+        csr = p.csr
+        nrows = max(1, int(round(csr.M * frac)))
+        rows = np.arange(0, csr.M, max(1, csr.M // nrows))[:nrows]
+        ro, ci, pos = oracle.select_rows(csr.row_offsets, csr.col_indices, rows)
+        vals = oracle.widen(csr.values, p.dtype)[pos]
+        B = oracle.widen(p.B, p.dtype)
+        X = oracle.widen(p.X, p.dtype)[rows]
+        Y = oracle.widen(p.Y, p.dtype)
+        t0 = time.perf_counter()
+        oracle.spmm(rows.size, csr.K, ro, ci, vals, B)
+        oracle.sddmm(rows.size, csr.K, ro, ci, X, Y)
+        secs += time.perf_counter() - t0
+        flops += 2 * 2.0 * pos.size * N_FFN
+    return flops, secs
+
+
+def cpu_baseline(frac, only=None):
+    import oracle
+    probs = problems(only)
+    flops, secs = oracle_sample_pass(probs, frac)
+    return {"value": round(flops / secs / 1e9, 3), "unit": "GFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"every launch of one step on a {frac:.4g} row sample (rows evenly spaced), "
+                      f"{flops / 1e9:.2f} GFLOP in {secs:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    if rank != 0:
+        return None
+    probs = problems()
+    frac = args.cpu_sample
+    for _ in range(args.warmup):
+        oracle_sample_pass(probs, frac / 4)
+    tot_f, tot_s = 0.0, 0.0
+    for _ in range(args.steps):
+        f, s = oracle_sample_pass(probs, frac)
+        tot_f += f
+        tot_s += s
+    value = tot_f / tot_s / 1e9
+    return {
+        "impl": "reference",
+        "metric": "SpMM/SDDMM useful GFLOP/s (2·nnz·N), HBM GB/s, % of roofline on 1 GB300",
+        "value": round(value, 3), "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot_s * 1e3 / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": f"{frac:.4g} of the rows of every launch per step"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": f"{frac:.4g} row sample of every launch, per step"},
+        "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", type=float, default=1.0 / 16)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="restrict to launches whose tag contains this (e.g. spmm:f32_4096x1024_s70); "
+                         "for profiling a single kernel, not a bench line")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
