@@ -114,6 +114,40 @@ int csr_sddmm(int M, int K, int D, int nnz,
               void *stream);
 
 /*
+ * csr_sddmm_static_scratch — csr_sddmm for callers that cannot allocate.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc (a plugin that only receives raw pointers from
+ * its host framework, a loop whose device memory was fixed at start-up, an
+ * environment that forbids allocation after initialisation) and so cannot
+ * supply csr_sddmm's workspace.  Same arguments, contract and result as
+ * csr_sddmm, minus the workspace: the scratch comes from one fixed 32 MiB
+ * array in the library's device image, which every GPU that loads the
+ * library holds until the process exits.
+ *
+ *   Limit: csr_sddmm_workspace_bytes(M, K, D, nnz, in_dtype) must not exceed
+ *          32 MiB (33554432 bytes); larger problems return USM_ERR_UNSUPPORTED
+ *          before anything is launched.  Problems that need no workspace
+ *          (one column strip) always fit.
+ *   Allocation: none, on any call (no cudaMalloc, cudaFree or allocating
+ *          library routine).
+ *   Set-up: the first call on a device (with that device current) looks up
+ *          the array's device address with cudaGetSymbolAddress and keeps it;
+ *          make that first call before any stream capture on the device.
+ *   Sharing: every call on a device uses the same array, which keeps the
+ *          last call's contents (nothing in it needs to start at zero).  Calls
+ *          whose executions overlap on the GPU (other streams, other host
+ *          threads) race on the array and give wrong results: serialise them.
+ */
+int csr_sddmm_static_scratch(int M, int K, int D, int nnz,
+                             const int *row_offsets, const int *col_indices,
+                             const int *row_swizzle,
+                             const void *X, int ldx,
+                             const void *Y, int ldy,
+                             void *out, usm_dtype in_dtype, usm_dtype out_dtype,
+                             void *stream);
+
+/*
  * row_swizzle_build — the row-swizzle processing order.
  *
  * Source: "Sparse GPU Kernels for Deep Learning", summary card, "Summary"

@@ -36,6 +36,7 @@ SIGNATURES = {
     "usm_poll_status": (_i, [_vp]),
     "usm_status_string": (ctypes.c_char_p, [_i]),
     "usm_selftest_wait_timeout": (_i, [_ll, _vp]),
+    "csr_sddmm_static_scratch": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _vp]),
 }
 
 _lib = None
