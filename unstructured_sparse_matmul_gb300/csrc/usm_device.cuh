@@ -106,6 +106,46 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float x) {
     return static_cast<uint16_t>(u >> 16);
 }
 
+// fp32 += bf16 × bf16 with the bf16 operands taken from halves of 32-bit
+// words (lo = bits 0..15, hi = bits 16..31).  fma.rn.f32.bf16 multiplies the
+// two bf16 values exactly and adds in fp32 with one rounding; on sm_103a it
+// issues at the full FP32 rate, so bf16 operands need no widening step.
+#define USM_FMA_BF16(NAME, AH, BH)                                                          \
+    __device__ __forceinline__ float NAME(uint32_t a, uint32_t b, float c) {               \
+        float d;                                                                           \
+        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"                                            \
+            "mov.b32 {a0, a1}, %1;\n\t"                                                     \
+            "mov.b32 {b0, b1}, %2;\n\t"                                                     \
+            "fma.rn.f32.bf16 %0, " AH ", " BH ", %3;\n\t}"                                  \
+            : "=f"(d)                                                                      \
+            : "r"(a), "r"(b), "f"(c));                                                     \
+        return d;                                                                          \
+    }
+USM_FMA_BF16(fma_bf16_hl, "a1", "b0")
+USM_FMA_BF16(fma_bf16_hh, "a1", "b1")
+USM_FMA_BF16(fma_bf16_ll, "a0", "b0")
+#undef USM_FMA_BF16
+
+// Shared-memory loads by 32-bit shared address.  volatile keeps them after
+// the barrier waits that publish the data they read.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 // Read-only streaming loads of CSR arrays.
 __device__ __forceinline__ int ldg_i32(const int* p) { return __ldg(p); }
 

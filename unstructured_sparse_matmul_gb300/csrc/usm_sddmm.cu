@@ -31,38 +31,31 @@
 namespace usm {
 namespace {
 
-template <bool BF, int L, int VV, int W, int KC>
+template <bool BF, int L, int VV, int W, int KC, int MINB>
 struct SddmmCfg {
-    static constexpr int EPV = BF ? 8 : 4;
+    static constexpr int EPV = BF ? 8 : 4;      // elements per 16-byte vector
     static constexpr int DT = L * VV * EPV;     // D columns per CTA
     static constexpr int G = 32 / L;
     static constexpr int PITCH = L * VV * 16;   // bytes per staged Y row
     static constexpr int STAGE = KC * PITCH;
-    static constexpr int BOX_ROWS = KC < 256 ? KC : 256;
+    static constexpr int BOX_ROWS = KC <= 256 ? KC : KC / 2;
     static constexpr int THREADS = W * 32;
     static constexpr int SMEM = 2 * STAGE + 64 + W * 32 * 4;
+    static constexpr int XW = VV * 4;           // 32-bit words of X per lane
     static_assert(G * L == 32, "groups must tile the warp");
-    static_assert(KC % BOX_ROWS == 0, "KC must be a multiple of the TMA box height");
+    static_assert(L == 8, "the list layout and reduction assume 8-lane groups");
+    static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
 };
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
 
 __device__ __forceinline__ int window_col(const SddmmArgs& a, int pos, int end, int lane) {
     const int p = pos + lane;
     return p < end ? __ldg(a.col_indices + p) : INT_MAX;
 }
 
-// X[r, d0 + j*L*EPV + l*EPV : +EPV] for j < VV as raw 32-bit words; zero
-// beyond D.
+// X[r, d0 + j*L*EPV + l*EPV : +EPV] for j < VV as raw 32-bit words (fp32
+// values, or packed bf16 pairs); zero beyond D or for a missing row.
 template <bool BF, int L, int VV>
-__device__ __forceinline__ void load_x(const SddmmArgs& a, int row, int d0, int l,
-                                       uint32_t (&xw)[VV * (BF ? 4 : 4)]) {
+__device__ __forceinline__ void load_x(const SddmmArgs& a, int row, int d0, int l, uint32_t (&xw)[VV * 4]) {
     constexpr int EPV = BF ? 8 : 4;
 #pragma unroll
     for (int j = 0; j < VV; ++j) {
@@ -101,12 +94,42 @@ __device__ __forceinline__ void load_x(const SddmmArgs& a, int row, int d0, int 
     }
 }
 
-template <bool BF, int L, int VV, int W, int KC>
-__global__ void __launch_bounds__(W * 32, 1)
+// Partial dot product of one lane: its X words with the 16-byte vectors of
+// one staged Y row.
+template <bool BF, int L, int VV>
+__device__ __forceinline__ float lane_dot(const uint32_t (&xw)[VV * 4], uint32_t yrow) {
+    if constexpr (BF) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < VV; ++j) {
+            const uint4 y = lds128(yrow + j * L * 16);
+            const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                s0 = fma_bf16_ll(xw[4 * j + q], yw[q], s0);
+                s1 = fma_bf16_hh(xw[4 * j + q], yw[q], s1);
+            }
+        }
+        return s0 + s1;
+    } else {
+        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < VV; ++j) {
+            const uint4 y = lds128(yrow + j * L * 16);
+            s2 = __ffma2_rn(make_float2(__uint_as_float(xw[4 * j]), __uint_as_float(xw[4 * j + 1])),
+                            make_float2(__uint_as_float(y.x), __uint_as_float(y.y)), s2);
+            s2 = __ffma2_rn(make_float2(__uint_as_float(xw[4 * j + 2]), __uint_as_float(xw[4 * j + 3])),
+                            make_float2(__uint_as_float(y.z), __uint_as_float(y.w)), s2);
+        }
+        return s2.x + s2.y;
+    }
+}
+
+template <bool BF, int L, int VV, int W, int KC, int MINB>
+__global__ void __launch_bounds__(W * 32, MINB)
     sddmm_kernel(const __grid_constant__ CUtensorMap tmY, const SddmmArgs a) {
-    using C_ = SddmmCfg<BF, L, VV, W, KC>;
-    constexpr int EPV = C_::EPV, G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE;
-    constexpr int NX = VV * EPV;  // X elements per lane
+    using C_ = SddmmCfg<BF, L, VV, W, KC, MINB>;
+    constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, XW = C_::XW;
 
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
@@ -190,10 +213,14 @@ __global__ void __launch_bounds__(W * 32, 1)
     int cur = my_start;
     // Prefetched state of the next row to process: its window and X strip.
     int pcol = window_col(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), lane);
-    uint32_t pxw[VV * 4];
+    uint32_t pxw[XW];
     load_x<BF, L, VV>(a, __shfl_sync(kFullMask, my_row, 0), d0, l, pxw);
 
     uint32_t* wl = lists + warp * 32;
+    // Entry e of a window goes to slot (e % G)·L + e / G, so group g finds
+    // its steps 0..L-1 contiguous at g·L and reads four per 128-bit load.
+    const int my_slot = (lane % G) * L + lane / G;
+    const uint32_t gl = smem_addr(wl + g * L);
     const bool single_strip = gridDim.y == 1;
 
     for (int j = 0; j < nchunks; ++j) {
@@ -208,21 +235,12 @@ __global__ void __launch_bounds__(W * 32, 1)
                 int rc = __shfl_sync(kFullMask, cur, i);
                 const int re = __shfl_sync(kFullMask, my_end, i);
                 int col = pcol;
-                float x[NX];
-                if (BF) {
+                uint32_t xw[XW];
 #pragma unroll
-                    for (int q = 0; q < NX / 2; ++q) {
-                        x[2 * q] = bf16lo(pxw[q]);
-                        x[2 * q + 1] = bf16hi(pxw[q]);
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < NX; ++q) x[q] = __uint_as_float(pxw[q]);
-                }
-                // Prefetch the next row slot (or slot 0 for the next chunk; its
-                // cursor is final once slot 0 has been processed, which holds
-                // when R > 1; for R == 1 the reload below after the segment
-                // covers it).
+                for (int q = 0; q < XW; ++q) xw[q] = pxw[q];
+                // Prefetch the next row slot (slot 0 for the next chunk: its
+                // cursor is final once slot 0 has been processed, when R > 1;
+                // for R == 1 the reload after the segment covers it).
                 {
                     const int ni = (i + 1 < R) ? i + 1 : 0;
                     if (ni != i) {
@@ -236,32 +254,20 @@ __global__ void __launch_bounds__(W * 32, 1)
                     const unsigned bal = __ballot_sync(kFullMask, valid);
                     const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);
                     if (n == 0) break;
-                    wl[lane] = (lane < n) ? (uint32_t)(col - k0) * PITCH : 0u;
+                    wl[my_slot] = (lane < n) ? (uint32_t)(col - k0) * PITCH : 0u;
                     __syncwarp();
                     float part[L];
 #pragma unroll
-                    for (int t = 0; t < L; ++t) {
-                        part[t] = 0.f;
-                        if (t * G < n) {
-                            const uint32_t off = wl[t * G + g];
-                            float2 s2 = make_float2(0.f, 0.f);
+                    for (int t4 = 0; t4 < L; t4 += 4) {
+                        if (t4 * G < n) {
+                            const uint4 o4 = lds128(gl + t4 * 4);
+                            const uint32_t off[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
-                            for (int jj = 0; jj < VV; ++jj) {
-                                const uint4 y = lds128(stage + off + jj * L * 16);
-                                if (BF) {
-                                    const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+                            for (int u = 0; u < 4; ++u)
+                                part[t4 + u] = ((t4 + u) * G < n) ? lane_dot<BF, L, VV>(xw, stage + off[u]) : 0.f;
+                        } else {
 #pragma unroll
-                                    for (int q = 0; q < 4; ++q)
-                                        s2 = __ffma2_rn(make_float2(x[jj * 8 + 2 * q], x[jj * 8 + 2 * q + 1]),
-                                                        make_float2(bf16lo(w[q]), bf16hi(w[q])), s2);
-                                } else {
-                                    s2 = __ffma2_rn(make_float2(x[jj * 4], x[jj * 4 + 1]),
-                                                    make_float2(__uint_as_float(y.x), __uint_as_float(y.y)), s2);
-                                    s2 = __ffma2_rn(make_float2(x[jj * 4 + 2], x[jj * 4 + 3]),
-                                                    make_float2(__uint_as_float(y.z), __uint_as_float(y.w)), s2);
-                                }
-                            }
-                            part[t] = s2.x + s2.y;
+                            for (int u = 0; u < 4; ++u) part[t4 + u] = 0.f;
                         }
                     }
                     // Transpose-reduce across the L lanes of each group: after it,
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(W * 32, 1)
                             part[q] = keep + __shfl_xor_sync(kFullMask, send, off);
                         }
                     }
-                    const int e = l * G + g;  // list entry whose sum this lane holds
+                    const int e = l * G + g;  // window entry whose sum this lane holds
                     if (e < n) {
                         const long long p = (long long)rc + e;
                         if (single_strip) {
@@ -341,12 +347,12 @@ __global__ void fill_out_kernel(void* out, long long n, int bf16) {
     }
 }
 
-template <bool BF, int L, int VV, int W, int KC>
+template <bool BF, int L, int VV, int W, int KC, int MINB>
 int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, cudaStream_t stream) {
-    using C_ = SddmmCfg<BF, L, VV, W, KC>;
+    using C_ = SddmmCfg<BF, L, VV, W, KC, MINB>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, Y, BF, a.K, a.D, ldy, C_::DT, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = sddmm_kernel<BF, L, VV, W, KC>;
+    auto kern = sddmm_kernel<BF, L, VV, W, KC, MINB>;
     static int configured_mask = 0;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -365,10 +371,11 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
         a.out = ws;
         a.out_stride = a.nnz;
     }
-    // Rows per warp: as many as keep ≥ 2 CTAs per SM in flight (up to 32).
+    // Rows per warp: as many as still give every SM ~4 CTAs over the launch
+    // (two resident at a time), up to 32.
     const int sms = sm_count_current_device();
     int R = 32;
-    while (R > 1 && (long long)((a.M + R * W - 1) / (R * W)) * nstrips < 2LL * sms) R >>= 1;
+    while (R > 1 && (long long)((a.M + R * W - 1) / (R * W)) * nstrips < 4LL * MINB * sms / 2) R >>= 1;
     a.rows_per_warp = R;
     const dim3 grid((a.M + R * W - 1) / (R * W), nstrips);
     kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);
@@ -409,9 +416,9 @@ int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream) {
 int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, size_t ws_bytes,
                  cudaStream_t stream) {
     constexpr int W = 16;
-    if (!in_bf16) return launch_cfg<false, 8, 4, W, 128>(a, Y, ldy, ws, ws_bytes, stream);
-    if (a.D <= 64) return launch_cfg<true, 8, 1, W, 512>(a, Y, ldy, ws, ws_bytes, stream);
-    return launch_cfg<true, 8, 2, W, 256>(a, Y, ldy, ws, ws_bytes, stream);
+    if (!in_bf16) return launch_cfg<false, 8, 4, W, 96, 2>(a, Y, ldy, ws, ws_bytes, stream);
+    if (a.D <= 64) return launch_cfg<true, 8, 1, W, 384, 2>(a, Y, ldy, ws, ws_bytes, stream);
+    return launch_cfg<true, 8, 2, W, 192, 2>(a, Y, ldy, ws, ws_bytes, stream);
 }
 
 }  // namespace usm

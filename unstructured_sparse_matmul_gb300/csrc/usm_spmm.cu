@@ -9,7 +9,9 @@
 // * 1-D tiles.  A CTA owns MT = R·W rows of A (taken in row-swizzle order,
 //   interleaved across its W warps so every warp gets a similar share) and
 //   one strip of NT output columns.  Each output element is accumulated by
-//   exactly one lane in a fixed order: results do not depend on the swizzle.
+//   exactly one lane group in a fixed order: results do not depend on the
+//   swizzle.  Two CTAs share an SM, so one CTA's barrier waits and prologue
+//   overlap the other's arithmetic.
 // * Dense operand staging.  The CTA walks K in chunks of KC rows.  For each
 //   chunk one thread issues TMA tensor copies of B[k0:k0+KC, n0:n0+NT] into a
 //   shared-memory stage (double buffered, completion on an mbarrier, bounded
@@ -17,20 +19,22 @@
 //   the CTA's rows are fetched, so block-diagonal (batched) matrices stay
 //   cheap.
 // * Sparse operand.  For each (row, chunk) a warp reads the next 32 column
-//   indices and values of the row with coalesced loads (the window of the
-//   row after its cursor, so a misaligned row start costs nothing), keeps the
-//   prefix whose columns fall in the chunk (ballot), and writes
-//   (byte offset into the stage, value) entries to a per-warp list.  The
-//   window of the next row is prefetched while the current row computes.
-// * Inner loop.  G = 32/L lane groups each take one list entry per step:
-//   every lane reads 16 bytes of the staged B row (one LDS.128; a group
-//   covers a whole 16·L-byte row, conflict-free) and does EPV FMAs into its
-//   accumulators (fp32 via packed f32x2 FMA; bf16 operands are widened
-//   exactly first).  At the end the G partial rows are added across groups.
+//   indices and values of the row with coalesced loads (the window after the
+//   row's cursor, so a misaligned row start costs nothing), keeps the prefix
+//   whose columns fall in the chunk (ballot) and writes (stage offset, value)
+//   entries to a per-warp list.  The next row's window is prefetched while
+//   the current one computes.
+// * Inner loop.  G = 32/L lane groups split the list into contiguous blocks.
+//   Four steps at a time a group reads its four entries with 128-bit
+//   broadcast loads, then each lane reads 16 (fp32) or 8 (bf16) bytes of the
+//   four staged B rows (a group covers whole rows, conflict-free) and does 4
+//   FMAs per row: packed f32x2 FMA for fp32, fma.rn.f32.bf16 straight on the
+//   bf16 halves for bf16.  The G partial rows are added across groups at the
+//   end.
 // * Accuracy.  In fp32 each (row, chunk) segment (≤ KC terms) is summed into
-//   a fresh accumulator that is then added to the row total, so every output
-//   is a sum of ≤ KC-term partials: the worst-case rounding bound stays
-//   below 1e-5·Σ|a||b| for K up to 4096 with KC = 128.
+//   a fresh accumulator that is then added to the row total: every output is
+//   a sum of ≤ KC-term partials, which keeps the worst-case rounding bound
+//   below 1e-5·Σ|a||b| for K up to 4096 (KC = 96).
 #include <climits>
 #include <type_traits>
 
@@ -40,42 +44,24 @@
 namespace usm {
 namespace {
 
-template <bool BF>
-struct SpmmEntry;
-template <>
-struct SpmmEntry<false> {  // fp32: byte offset, value bits
-    using T = uint2;
-};
-template <>
-struct SpmmEntry<true> {  // bf16: (byte offset / 16) | bf16 value << 16
-    using T = uint32_t;
-};
-
 template <bool BF, int L, int R, int W, int KC>
 struct SpmmCfg {
-    static constexpr int EPV = BF ? 8 : 4;  // elements per 16-byte vector
-    static constexpr int NT = L * EPV;      // output columns per CTA
-    static constexpr int G = 32 / L;        // nonzeros per warp step
-    static constexpr int PITCH = L * 16;    // bytes per staged B row
+    static constexpr int ES = BF ? 2 : 4;          // element bytes
+    static constexpr int NT = L * 4;               // output columns per CTA (4 per lane)
+    static constexpr int G = 32 / L;               // lane groups (nonzeros per warp step)
+    static constexpr int LANE_BYTES = 4 * ES;      // B bytes per lane per step
+    static constexpr int PITCH = L * LANE_BYTES;   // bytes per staged B row
     static constexpr int STAGE = KC * PITCH;
     static constexpr int MT = R * W;
-    static constexpr int BOX_ROWS = KC < 256 ? KC : 256;
+    static constexpr int BOX_ROWS = KC <= 256 ? KC : KC / 2;
     static constexpr int THREADS = W * 32;
-    using Entry = typename SpmmEntry<BF>::T;
-    static constexpr int LIST_BYTES = W * 32 * (int)sizeof(Entry);
+    static constexpr int ENTRY = BF ? 4 : 8;       // list entry bytes
+    static constexpr int LIST_BYTES = W * 32 * ENTRY;
     static constexpr int SMEM = 2 * STAGE + 64 + LIST_BYTES;
     static_assert(32 % L == 0, "L must divide the warp");
-    static_assert(KC % BOX_ROWS == 0, "KC must be a multiple of the TMA box height");
-    static_assert(STAGE <= 65536 * 16, "stage offsets must fit the entry encoding");
+    static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
+    static_assert(!BF || STAGE / 8 < 65536, "bf16 entry offsets are 16-bit multiples of 8 bytes");
 };
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
 
 // Window of 32 consecutive nonzeros of a row starting at `pos`: lane i gets
 // nonzero pos+i (column INT_MAX past the row end).
@@ -96,17 +82,16 @@ __device__ __forceinline__ void load_window(const SpmmArgs& a, int pos, int end,
 }
 
 template <bool BF, int L, int R, int W, int KC>
-__global__ void __launch_bounds__(W * 32, 1)
+__global__ void __launch_bounds__(W * 32, 2)
     spmm_kernel(const __grid_constant__ CUtensorMap tmB, const SpmmArgs a) {
     using C_ = SpmmCfg<BF, L, R, W, KC>;
-    using Entry = typename C_::Entry;
-    constexpr int EPV = C_::EPV, G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE;
+    constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, ENTRY = C_::ENTRY;
 
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * STAGE);
     int* kr = reinterpret_cast<int*>(smem + 2 * STAGE + 16);  // [0]=min col, [1]=max col, [2]=abort
-    Entry* lists = reinterpret_cast<Entry*>(smem + 2 * STAGE + 64);
+    unsigned char* lists = smem + 2 * STAGE + 64;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / L, l = lane % L;
@@ -179,11 +164,11 @@ __global__ void __launch_bounds__(W * 32, 1)
         if (nchunks > 1) issue(1);
     }
 
-    float acc[R][EPV];
+    float acc[R][4];
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int v = 0; v < EPV; ++v) acc[i][v] = 0.f;
+        for (int v = 0; v < 4; ++v) acc[i][v] = 0.f;
 
     int cur = my_start;  // lane i: cursor of row slot i
     int pcol;
@@ -191,18 +176,15 @@ __global__ void __launch_bounds__(W * 32, 1)
     load_window<BF>(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), lane, pcol,
                     pval);
 
-    Entry* wl = lists + warp * 32;
-    bool timed_out = false;
+    unsigned char* wl = lists + warp * 32 * ENTRY;
+    const uint32_t wl_addr = smem_addr(wl);
 
     for (int j = 0; j < nchunks; ++j) {
         const int s = j & 1;
         const int k0 = (c_lo + j) * KC;
         const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j >> 1) & 1, kWaitLimitNs);
-        if (!ok) {
-            timed_out = true;
-            kr[2] = 1;
-        }
-        const uint32_t stage = smem_addr(stages + s * STAGE) + l * 16;
+        if (!ok) kr[2] = 1;
+        const uint32_t stage = smem_addr(stages + s * STAGE) + l * C_::LANE_BYTES;
         if (ok) {
 #pragma unroll
             for (int i = 0; i < R; ++i) {
@@ -213,53 +195,60 @@ __global__ void __launch_bounds__(W * 32, 1)
                 if (i + 1 < R)
                     load_window<BF>(a, __shfl_sync(kFullMask, cur, i + 1),
                                     __shfl_sync(kFullMask, my_end, i + 1), lane, pcol, pval);
-                float accc[EPV];
-#pragma unroll
-                for (int v = 0; v < EPV; ++v) accc[v] = 0.f;
+                float c4[4] = {0.f, 0.f, 0.f, 0.f};  // fp32: this segment's partial sums
                 while (true) {
                     const bool valid = (rc + lane < re) && ((unsigned)(col - k0) < (unsigned)KC);
                     const unsigned bal = __ballot_sync(kFullMask, valid);
                     const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);  // valid prefix
                     if (n == 0) break;
-                    const int npad = (n + G - 1) / G * G;
+                    const int npad = (n + 4 * G - 1) / (4 * G) * (4 * G);
                     if (lane < npad) {
                         const bool live = lane < n;
                         const uint32_t off = live ? (uint32_t)(col - k0) * PITCH : 0u;
                         if constexpr (BF) {
-                            wl[lane] = live ? ((off >> 4) | (val << 16)) : 0u;
+                            reinterpret_cast<uint32_t*>(wl)[lane] = live ? ((off >> 3) | (val << 16)) : 0u;
                         } else {
-                            wl[lane] = live ? make_uint2(off, val) : make_uint2(0u, 0u);
+                            reinterpret_cast<uint2*>(wl)[lane] = live ? make_uint2(off, val) : make_uint2(0u, 0u);
                         }
                     }
                     __syncwarp();
-#pragma unroll 4
-                    for (int t = g; t < npad; t += G) {
+                    const int q = npad / G;  // steps of each group, multiple of 4
+                    const uint32_t gl = wl_addr + g * q * ENTRY;
+#pragma unroll 1
+                    for (int t = 0; t < q; t += 4) {
                         if constexpr (BF) {
-                            const uint32_t e = wl[t];
-                            const uint4 b = lds128(stage + ((e & 0xffffu) << 4));
-                            const float av = __uint_as_float(e & 0xffff0000u);
-                            const float2 a2 = make_float2(av, av);
-                            const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+                            const uint4 e = lds128(gl + t * 4);
+                            const uint32_t ev[4] = {e.x, e.y, e.z, e.w};
+                            uint2 b[4];
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                float2 c2 = make_float2(acc[i][2 * q], acc[i][2 * q + 1]);
-                                c2 = __ffma2_rn(a2, make_float2(bf16lo(w[q]), bf16hi(w[q])), c2);
-                                acc[i][2 * q] = c2.x;
-                                acc[i][2 * q + 1] = c2.y;
+                            for (int u = 0; u < 4; ++u) b[u] = lds64(stage + ((ev[u] & 0xffffu) << 3));
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                acc[i][0] = fma_bf16_hl(ev[u], b[u].x, acc[i][0]);
+                                acc[i][1] = fma_bf16_hh(ev[u], b[u].x, acc[i][1]);
+                                acc[i][2] = fma_bf16_hl(ev[u], b[u].y, acc[i][2]);
+                                acc[i][3] = fma_bf16_hh(ev[u], b[u].y, acc[i][3]);
                             }
                         } else {
-                            const uint2 e = wl[t];
-                            const uint4 b = lds128(stage + e.x);
-                            const float av = __uint_as_float(e.y);
-                            const float2 a2 = make_float2(av, av);
-                            float2 c0 = make_float2(accc[0], accc[1]);
-                            float2 c1 = make_float2(accc[2], accc[3]);
-                            c0 = __ffma2_rn(a2, make_float2(__uint_as_float(b.x), __uint_as_float(b.y)), c0);
-                            c1 = __ffma2_rn(a2, make_float2(__uint_as_float(b.z), __uint_as_float(b.w)), c1);
-                            accc[0] = c0.x;
-                            accc[1] = c0.y;
-                            accc[2] = c1.x;
-                            accc[3] = c1.y;
+                            const uint4 e01 = lds128(gl + t * 8);
+                            const uint4 e23 = lds128(gl + t * 8 + 16);
+                            const uint32_t off[4] = {e01.x, e01.z, e23.x, e23.z};
+                            const uint32_t av[4] = {e01.y, e01.w, e23.y, e23.w};
+                            uint4 b[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) b[u] = lds128(stage + off[u]);
+                            float2 lo = make_float2(c4[0], c4[1]), hi = make_float2(c4[2], c4[3]);
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const float x = __uint_as_float(av[u]);
+                                const float2 a2 = make_float2(x, x);
+                                lo = __ffma2_rn(a2, make_float2(__uint_as_float(b[u].x), __uint_as_float(b[u].y)), lo);
+                                hi = __ffma2_rn(a2, make_float2(__uint_as_float(b[u].z), __uint_as_float(b[u].w)), hi);
+                            }
+                            c4[0] = lo.x;
+                            c4[1] = lo.y;
+                            c4[2] = hi.x;
+                            c4[3] = hi.y;
                         }
                     }
                     __syncwarp();
@@ -269,7 +258,7 @@ __global__ void __launch_bounds__(W * 32, 1)
                 }
                 if constexpr (!BF) {
 #pragma unroll
-                    for (int v = 0; v < EPV; ++v) acc[i][v] += accc[v];
+                    for (int v = 0; v < 4; ++v) acc[i][v] += c4[v];
                 }
                 if (lane == i) cur = rc;
                 if (i + 1 == R)
@@ -290,14 +279,13 @@ __global__ void __launch_bounds__(W * 32, 1)
         // still in flight so none lands after the CTA exits, and leave.
         if (threadIdx.x == 0) {
             record_status(a.status, USM_ERR_TIMEOUT);
-            for (int j = 0; j < nchunks && j < 2; ++j) {
-                // Stages hold chunks whose phases are unknown here; wait on both
-                // parities briefly (each wait ends by itself).
-                mbar_wait_bounded(smem_addr(&bars[j]), 0, 1000000ull);
-                mbar_wait_bounded(smem_addr(&bars[j]), 1, 1000000ull);
+            for (int b = 0; b < nchunks && b < 2; ++b) {
+                // Waiting on both parities waits for the barrier's current phase
+                // (the other parity reports complete at once); each wait is bounded.
+                mbar_wait_bounded(smem_addr(&bars[b]), 0, 1000000ull);
+                mbar_wait_bounded(smem_addr(&bars[b]), 1, 1000000ull);
             }
         }
-        (void)timed_out;
         return;
     }
 
@@ -305,7 +293,7 @@ __global__ void __launch_bounds__(W * 32, 1)
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int v = 0; v < EPV; ++v) {
+        for (int v = 0; v < 4; ++v) {
             float x = acc[i][v];
             if (G >= 2) x += __shfl_xor_sync(kFullMask, x, L);
             if (G >= 4) x += __shfl_xor_sync(kFullMask, x, 2 * L);
@@ -317,16 +305,13 @@ __global__ void __launch_bounds__(W * 32, 1)
     for (int i = 0; i < R; ++i) {
         const int row = __shfl_sync(kFullMask, my_row, i);
         if (row < 0 || g != 0) continue;
-        const int c0 = n0 + l * EPV;
+        const int c0 = n0 + l * 4;
         float* dst = a.C + (long long)row * a.ldc + c0;
-        if (c0 + EPV <= a.N) {
-#pragma unroll
-            for (int v = 0; v < EPV; v += 4)
-                *reinterpret_cast<float4*>(dst + v) =
-                    make_float4(acc[i][v], acc[i][v + 1], acc[i][v + 2], acc[i][v + 3]);
+        if (c0 + 4 <= a.N) {
+            *reinterpret_cast<float4*>(dst) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
         } else {
 #pragma unroll
-            for (int v = 0; v < EPV; ++v)
+            for (int v = 0; v < 4; ++v)
                 if (c0 + v < a.N) dst[v] = acc[i][v];
         }
     }
@@ -375,29 +360,17 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
     return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
 }
 
-// Tile choice: the widest column strip the lanes can cover without waste,
-// and the most rows per CTA (best reuse of each staged B chunk) that still
-// gives every SM at least ~2 CTAs.
+// Tile choice: 128 output columns per CTA (4 per lane), or 64 when N ≤ 64;
+// 4 rows per warp and 16 warps (64 rows per CTA), two CTAs per SM; stages
+// of 48 KB.
 int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
-    const int sms = sm_count_current_device();
-    auto ctas = [&](int nt, int mt) {
-        return (long long)((a.N + nt - 1) / nt) * ((a.M + mt - 1) / mt);
-    };
-    constexpr int W = 16;
+    constexpr int W = 16, R = 4;
     if (!bf16) {
-        if (a.N <= 64) {
-            if (ctas(64, 8 * W) >= 2 * sms) return launch_cfg<false, 16, 8, W, 256>(a, B, ldb, stream);
-            return launch_cfg<false, 16, 4, W, 256>(a, B, ldb, stream);
-        }
-        if (ctas(128, 8 * W) >= 2 * sms) return launch_cfg<false, 32, 8, W, 128>(a, B, ldb, stream);
-        return launch_cfg<false, 32, 4, W, 128>(a, B, ldb, stream);
+        if (a.N <= 64) return launch_cfg<false, 16, R, W, 192>(a, B, ldb, stream);
+        return launch_cfg<false, 32, R, W, 96>(a, B, ldb, stream);
     }
-    if (a.N <= 64) {
-        if (ctas(64, 8 * W) >= 2 * sms) return launch_cfg<true, 8, 8, W, 512>(a, B, ldb, stream);
-        return launch_cfg<true, 8, 4, W, 512>(a, B, ldb, stream);
-    }
-    if (ctas(256, 8 * W) >= 2 * sms) return launch_cfg<true, 32, 8, W, 128>(a, B, ldb, stream);
-    return launch_cfg<true, 32, 4, W, 128>(a, B, ldb, stream);
+    if (a.N <= 64) return launch_cfg<true, 16, R, W, 384>(a, B, ldb, stream);
+    return launch_cfg<true, 32, R, W, 192>(a, B, ldb, stream);
 }
 
 }  // namespace usm
