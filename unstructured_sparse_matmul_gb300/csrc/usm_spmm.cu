@@ -14,8 +14,8 @@
 //   overlap the other's arithmetic.
 // * Dense operand staging.  The CTA walks K in chunks of KC rows.  For each
 //   chunk one thread issues TMA tensor copies of B[k0:k0+KC, n0:n0+NT] into a
-//   shared-memory stage (double buffered, completion on an mbarrier, bounded
-//   wait).  Only the chunks between the smallest and largest column index of
+//   shared-memory stage (completion on an mbarrier, bounded wait; one or two
+//   stages).  Only the chunks between the smallest and largest column index of
 //   the CTA's rows are fetched, so block-diagonal (batched) matrices stay
 //   cheap.
 // * Sparse operand.  For each (row, chunk) a warp reads the next 32 column
@@ -26,15 +26,16 @@
 //   the current one computes.
 // * Inner loop.  G = 32/L lane groups split the list into contiguous blocks.
 //   Four steps at a time a group reads its four entries with 128-bit
-//   broadcast loads, then each lane reads 16 (fp32) or 8 (bf16) bytes of the
-//   four staged B rows (a group covers whole rows, conflict-free) and does 4
-//   FMAs per row: packed f32x2 FMA for fp32, fma.rn.f32.bf16 straight on the
-//   bf16 halves for bf16.  The G partial rows are added across groups at the
-//   end.
-// * Accuracy.  In fp32 each (row, chunk) segment (≤ KC terms) is summed into
-//   a fresh accumulator that is then added to the row total: every output is
-//   a sum of ≤ KC-term partials, which keeps the worst-case rounding bound
-//   below 1e-5·Σ|a||b| for K up to 4096 (KC = 96).
+//   broadcast loads (then 0-3 single steps), each lane reads 16 (fp32) or 8
+//   (bf16) bytes of the staged B row (a group covers whole rows,
+//   conflict-free) and does 4 FMAs: packed f32x2 FMA for fp32,
+//   fma.rn.f32.bf16 on the bf16 halves for bf16.  The G partial rows are
+//   added across groups at the end.
+// * Accuracy.  In fp32 each window of ≤ 32 nonzeros is summed into a fresh
+//   accumulator, windows are added into a per-(row, chunk) partial and those
+//   into the row total: with ≤ 32 + 7 + K/KC additions along any output's
+//   path the worst-case rounding bound stays below 1e-5·Σ|a||b| while
+//   K/KC ≤ 128 (K up to 12288 with KC = 96).
 #include <climits>
 #include <type_traits>
 
@@ -44,7 +45,7 @@
 namespace usm {
 namespace {
 
-template <bool BF, int L, int R, int W, int KC>
+template <bool BF, int L, int R, int W, int KC, int NS>
 struct SpmmCfg {
     static constexpr int ES = BF ? 2 : 4;          // element bytes
     static constexpr int NT = L * 4;               // output columns per CTA (4 per lane)
@@ -53,11 +54,12 @@ struct SpmmCfg {
     static constexpr int PITCH = L * LANE_BYTES;   // bytes per staged B row
     static constexpr int STAGE = KC * PITCH;
     static constexpr int MT = R * W;
-    static constexpr int BOX_ROWS = KC <= 256 ? KC : KC / 2;
+    static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
     static constexpr int THREADS = W * 32;
     static constexpr int ENTRY = BF ? 4 : 8;       // list entry bytes
     static constexpr int LIST_BYTES = W * 32 * ENTRY;
-    static constexpr int SMEM = 2 * STAGE + 64 + LIST_BYTES;
+    static constexpr int SMEM = NS * STAGE + 64 + LIST_BYTES;
+    static_assert(NS == 1 || NS == 2, "one or two stages");
     static_assert(32 % L == 0, "L must divide the warp");
     static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
     static_assert(!BF || STAGE / 8 < 65536, "bf16 entry offsets are 16-bit multiples of 8 bytes");
@@ -81,17 +83,17 @@ __device__ __forceinline__ void load_window(const SpmmArgs& a, int pos, int end,
     }
 }
 
-template <bool BF, int L, int R, int W, int KC>
+template <bool BF, int L, int R, int W, int KC, int NS>
 __global__ void __launch_bounds__(W * 32, 2)
     spmm_kernel(const __grid_constant__ CUtensorMap tmB, const SpmmArgs a) {
-    using C_ = SpmmCfg<BF, L, R, W, KC>;
+    using C_ = SpmmCfg<BF, L, R, W, KC, NS>;
     constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, ENTRY = C_::ENTRY;
 
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * STAGE);
-    int* kr = reinterpret_cast<int*>(smem + 2 * STAGE + 16);  // [0]=min col, [1]=max col, [2]=abort
-    unsigned char* lists = smem + 2 * STAGE + 64;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
+    int* kr = reinterpret_cast<int*>(smem + NS * STAGE + 16);  // [0]=min col, [1]=max col, [2]=abort
+    unsigned char* lists = smem + NS * STAGE + 64;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / L, l = lane % L;
@@ -150,7 +152,7 @@ __global__ void __launch_bounds__(W * 32, 2)
     }
 
     auto issue = [&](int j) {
-        const int s = j & 1;
+        const int s = j % NS;
         const uint32_t bar = smem_addr(&bars[s]);
         mbar_arrive_expect_tx(bar, STAGE);
         const uint32_t dst = smem_addr(stages + s * STAGE);
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(W * 32, 2)
     };
     if (threadIdx.x == 0) {
         if (nchunks > 0) issue(0);
-        if (nchunks > 1) issue(1);
+        if (NS > 1 && nchunks > 1) issue(1);
     }
 
     float acc[R][4];
@@ -180,9 +182,9 @@ __global__ void __launch_bounds__(W * 32, 2)
     const uint32_t wl_addr = smem_addr(wl);
 
     for (int j = 0; j < nchunks; ++j) {
-        const int s = j & 1;
+        const int s = j % NS;
         const int k0 = (c_lo + j) * KC;
-        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j >> 1) & 1, kWaitLimitNs);
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs);
         if (!ok) kr[2] = 1;
         const uint32_t stage = smem_addr(stages + s * STAGE) + l * C_::LANE_BYTES;
         if (ok) {
@@ -195,13 +197,17 @@ __global__ void __launch_bounds__(W * 32, 2)
                 if (i + 1 < R)
                     load_window<BF>(a, __shfl_sync(kFullMask, cur, i + 1),
                                     __shfl_sync(kFullMask, my_end, i + 1), lane, pcol, pval);
-                float c4[4] = {0.f, 0.f, 0.f, 0.f};  // fp32: this segment's partial sums
+                float c4[4] = {0.f, 0.f, 0.f, 0.f};  // fp32: this window's partial sums (≤ 32 terms)
+                float cc[4] = {0.f, 0.f, 0.f, 0.f};  // fp32: this chunk segment's windows
                 while (true) {
                     const bool valid = (rc + lane < re) && ((unsigned)(col - k0) < (unsigned)KC);
                     const unsigned bal = __ballot_sync(kFullMask, valid);
                     const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);  // valid prefix
                     if (n == 0) break;
-                    const int npad = (n + 4 * G - 1) / (4 * G) * (4 * G);
+                    // G == 1: exact count (0-3 single steps at the end).  G > 1: each
+                    // group's block must start 16-byte aligned for the 128-bit
+                    // entry loads, so pad to a multiple of 4·G.
+                    const int npad = (G == 1) ? n : (n + 4 * G - 1) / (4 * G) * (4 * G);
                     if (lane < npad) {
                         const bool live = lane < n;
                         const uint32_t off = live ? (uint32_t)(col - k0) * PITCH : 0u;
@@ -212,53 +218,73 @@ __global__ void __launch_bounds__(W * 32, 2)
                         }
                     }
                     __syncwarp();
-                    const int q = npad / G;  // steps of each group, multiple of 4
+                    const int q = npad / G;  // steps of each group
+                    const int q4 = q & ~3;
                     const uint32_t gl = wl_addr + g * q * ENTRY;
+                    // One bf16 step: entry e = (stage offset / 8) | value << 16.
+                    auto step_bf16 = [&](uint32_t e) {
+                        const uint2 b = lds64(stage + ((e & 0xffffu) << 3));
+                        const uint16_t av = hi16(e);
+                        acc[i][0] = fma_bf16(av, lo16(b.x), acc[i][0]);
+                        acc[i][1] = fma_bf16(av, hi16(b.x), acc[i][1]);
+                        acc[i][2] = fma_bf16(av, lo16(b.y), acc[i][2]);
+                        acc[i][3] = fma_bf16(av, hi16(b.y), acc[i][3]);
+                    };
+                    // One fp32 step: staged row at byte offset off, value bits av.
+                    auto step_f32 = [&](const uint4& b, uint32_t av) {
+                        const float x = __uint_as_float(av);
+                        const float2 a2 = make_float2(x, x);
+                        float2 lo = make_float2(c4[0], c4[1]), hi = make_float2(c4[2], c4[3]);
+                        lo = __ffma2_rn(a2, make_float2(__uint_as_float(b.x), __uint_as_float(b.y)), lo);
+                        hi = __ffma2_rn(a2, make_float2(__uint_as_float(b.z), __uint_as_float(b.w)), hi);
+                        c4[0] = lo.x;
+                        c4[1] = lo.y;
+                        c4[2] = hi.x;
+                        c4[3] = hi.y;
+                    };
 #pragma unroll 1
-                    for (int t = 0; t < q; t += 4) {
+                    for (int t = 0; t < q4; t += 4) {
                         if constexpr (BF) {
                             const uint4 e = lds128(gl + t * 4);
-                            const uint32_t ev[4] = {e.x, e.y, e.z, e.w};
-                            uint2 b[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) b[u] = lds64(stage + ((ev[u] & 0xffffu) << 3));
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                acc[i][0] = fma_bf16_hl(ev[u], b[u].x, acc[i][0]);
-                                acc[i][1] = fma_bf16_hh(ev[u], b[u].x, acc[i][1]);
-                                acc[i][2] = fma_bf16_hl(ev[u], b[u].y, acc[i][2]);
-                                acc[i][3] = fma_bf16_hh(ev[u], b[u].y, acc[i][3]);
-                            }
+                            step_bf16(e.x);
+                            step_bf16(e.y);
+                            step_bf16(e.z);
+                            step_bf16(e.w);
                         } else {
                             const uint4 e01 = lds128(gl + t * 8);
                             const uint4 e23 = lds128(gl + t * 8 + 16);
-                            const uint32_t off[4] = {e01.x, e01.z, e23.x, e23.z};
-                            const uint32_t av[4] = {e01.y, e01.w, e23.y, e23.w};
-                            uint4 b[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) b[u] = lds128(stage + off[u]);
-                            float2 lo = make_float2(c4[0], c4[1]), hi = make_float2(c4[2], c4[3]);
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const float x = __uint_as_float(av[u]);
-                                const float2 a2 = make_float2(x, x);
-                                lo = __ffma2_rn(a2, make_float2(__uint_as_float(b[u].x), __uint_as_float(b[u].y)), lo);
-                                hi = __ffma2_rn(a2, make_float2(__uint_as_float(b[u].z), __uint_as_float(b[u].w)), hi);
-                            }
-                            c4[0] = lo.x;
-                            c4[1] = lo.y;
-                            c4[2] = hi.x;
-                            c4[3] = hi.y;
+                            const uint4 b0 = lds128(stage + e01.x), b1 = lds128(stage + e01.z);
+                            const uint4 b2 = lds128(stage + e23.x), b3 = lds128(stage + e23.z);
+                            step_f32(b0, e01.y);
+                            step_f32(b1, e01.w);
+                            step_f32(b2, e23.y);
+                            step_f32(b3, e23.w);
+                        }
+                    }
+#pragma unroll 1
+                    for (int t = q4; t < q; ++t) {  // 0-3 remaining steps (G == 1 only)
+                        if constexpr (BF) {
+                            step_bf16(lds32(gl + t * 4));
+                        } else {
+                            const uint2 e = lds64(gl + t * 8);
+                            step_f32(lds128(stage + e.x), e.y);
                         }
                     }
                     __syncwarp();
+                    if constexpr (!BF) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            cc[v] += c4[v];
+                            c4[v] = 0.f;
+                        }
+                    }
                     rc += n;
                     if (n < 32) break;
                     load_window<BF>(a, rc, re, lane, col, val);
                 }
                 if constexpr (!BF) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) acc[i][v] += c4[v];
+                    for (int v = 0; v < 4; ++v) acc[i][v] += cc[v];
                 }
                 if (lane == i) cur = rc;
                 if (i + 1 == R)
@@ -268,9 +294,9 @@ __global__ void __launch_bounds__(W * 32, 2)
         }
         __syncthreads();  // every warp is done with stage s
         if (kr[2]) break;
-        if (threadIdx.x == 0 && j + 2 < nchunks) {
+        if (threadIdx.x == 0 && j + NS < nchunks) {
             fence_proxy_async_smem();
-            issue(j + 2);
+            issue(j + NS);
         }
     }
 
@@ -279,7 +305,7 @@ __global__ void __launch_bounds__(W * 32, 2)
         // still in flight so none lands after the CTA exits, and leave.
         if (threadIdx.x == 0) {
             record_status(a.status, USM_ERR_TIMEOUT);
-            for (int b = 0; b < nchunks && b < 2; ++b) {
+            for (int b = 0; b < nchunks && b < NS; ++b) {
                 // Waiting on both parities waits for the barrier's current phase
                 // (the other parity reports complete at once); each wait is bounded.
                 mbar_wait_bounded(smem_addr(&bars[b]), 0, 1000000ull);
@@ -326,12 +352,12 @@ __global__ void fill_f32_kernel(float* C, int M, int N, long long ldc) {
     }
 }
 
-template <bool BF, int L, int R, int W, int KC>
+template <bool BF, int L, int R, int W, int KC, int NS>
 int launch_cfg(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
-    using C_ = SpmmCfg<BF, L, R, W, KC>;
+    using C_ = SpmmCfg<BF, L, R, W, KC, NS>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::NT, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = spmm_kernel<BF, L, R, W, KC>;
+    auto kern = spmm_kernel<BF, L, R, W, KC, NS>;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -361,16 +387,22 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 }
 
 // Tile choice: 128 output columns per CTA (4 per lane), or 64 when N ≤ 64;
-// 4 rows per warp and 16 warps (64 rows per CTA), two CTAs per SM; stages
-// of 48 KB.
+// 4 rows per warp and 16 warps (64 rows per CTA), two CTAs per SM and one
+// 96 KB stage per CTA: while one CTA waits for its next chunk the other
+// computes, and the tall chunks (KC = 192 fp32 / 384 bf16 rows) halve the
+// per-(row, chunk) work that a double-buffered 2 x 48 KB layout needs
+// (measured: FFN step 7.69 against 8.90 ms).
+#ifndef USM_SPMM_STAGES
+#define USM_SPMM_STAGES 1
+#endif
 int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
-    constexpr int W = 16, R = 4;
+    constexpr int W = 16, R = 4, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
     if (!bf16) {
-        if (a.N <= 64) return launch_cfg<false, 16, R, W, 192>(a, B, ldb, stream);
-        return launch_cfg<false, 32, R, W, 96>(a, B, ldb, stream);
+        if (a.N <= 64) return launch_cfg<false, 16, R, W, 192 * F, NS>(a, B, ldb, stream);
+        return launch_cfg<false, 32, R, W, 96 * F, NS>(a, B, ldb, stream);
     }
-    if (a.N <= 64) return launch_cfg<true, 16, R, W, 384>(a, B, ldb, stream);
-    return launch_cfg<true, 32, R, W, 192>(a, B, ldb, stream);
+    if (a.N <= 64) return launch_cfg<true, 16, R, W, 384 * F, NS>(a, B, ldb, stream);
+    return launch_cfg<true, 32, R, W, 192 * F, NS>(a, B, ldb, stream);
 }
 
 }  // namespace usm
