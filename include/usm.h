@@ -171,6 +171,81 @@ int row_swizzle_build(int M, int K, int seg_rows, const int *row_offsets, int *s
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * csr_sddmm_general — SDDMM with the element-wise scaling and operand
+ * orientation the specialised form drops.
+ *
+ * Source: "Sparse GPU Kernels for Deep Learning", summary card, "Interesting
+ * ideas" I3 (the general case, which the authors note is easy to add).
+ *
+ *   out[p] = s_p · Σ_{j<D} X[r][j] · Yop[col_indices[p]][j],  p in row r,
+ *   s_p = values[p] (mask values, `in_dtype`) or 1 when values is NULL,
+ *   Yop = Y when y_transposed = 1 (Y is K×D, ldy ≥ D, as csr_sddmm), or
+ *   Yop = Yᵀ when y_transposed = 0 (Y is D×K row-major, ldy ≥ K; it is
+ *   transposed into the workspace first, so it has no alignment rule).
+ *   The scaling multiplies the fp32 dot product once (one extra rounding).
+ *   workspace : csr_sddmm_general_workspace_bytes(M, K, D, nnz, in_dtype,
+ *           y_transposed) bytes, 256-byte aligned, contents ignored.
+ * Other arguments, limits and empty cases as csr_sddmm.
+ */
+size_t csr_sddmm_general_workspace_bytes(int M, int K, int D, int nnz, usm_dtype in_dtype, int y_transposed);
+
+int csr_sddmm_general(int M, int K, int D, int nnz,
+                      const int *row_offsets, const int *col_indices, const void *values,
+                      const int *row_swizzle,
+                      const void *X, int ldx,
+                      const void *Y, int ldy, int y_transposed,
+                      void *out, usm_dtype in_dtype, usm_dtype out_dtype,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * csr_row_softmax — softmax over the stored entries of each CSR row:
+ *   out[p] = exp(s[p] - m_r) / Σ_{q in row r} exp(s[q] - m_r),  m_r = max_q s[q],
+ * scores fp32 [nnz], out fp32 or bf16 (nearest even) [nnz]; empty rows write
+ * nothing.  The normalisation step between the SDDMM scores and the SpMM of
+ * sparse attention (the sparse-attention use of the kernels, "Interesting
+ * ideas" I3).  Rounding: ≤ n/32 + 8 fp32 roundings per output for a row of n
+ * entries (lane sums, a 5-level tree, exp and one division).
+ */
+int csr_row_softmax(int M, int nnz, const int *row_offsets, const float *scores, void *out,
+                    usm_dtype out_dtype, void *stream);
+
+/*
+ * csr_transpose — Aᵀ in CSR, for the sparse layer's input gradient.
+ *
+ * Source: "Sparse GPU Kernels for Deep Learning", summary card, "Summary"
+ * (the kernels serve training as well as inference; the input gradient of a
+ * sparse layer C = A·B is dB = Aᵀ·dC, an SpMM on the transposed weight).
+ *
+ *   A     : M×K, CSR (row_offsets, col_indices, values of `dtype`; values may
+ *           be NULL to transpose the structure only, then values_t is NULL).
+ *   Aᵀ    : K×M, CSR written to row_offsets_t[K+1], col_indices_t[nnz] and
+ *           values_t[nnz].  Each row of Aᵀ lists its column indices (rows of
+ *           A) in increasing order, so the result is unique and bit-exact.
+ *   perm_out : NULL, or int32[nnz] receiving, for each nonzero q of Aᵀ, the
+ *           position in A's arrays it came from (values_t[q] = values[perm[q]]);
+ *           csr_permute_values re-gathers new values with it.
+ *   workspace : at least csr_transpose_workspace_bytes(M, K, nnz) bytes of
+ *           device scratch, 256-byte aligned (contents ignored on entry).
+ * Column indices outside [0, K) are clamped (contract violations give
+ * undefined but in-bounds results).  nnz = 0 writes row_offsets_t = 0.
+ */
+size_t csr_transpose_workspace_bytes(int M, int K, int nnz);
+
+int csr_transpose(int M, int K, int nnz,
+                  const int *row_offsets, const int *col_indices, const void *values,
+                  usm_dtype dtype,
+                  int *row_offsets_t, int *col_indices_t, void *values_t, int *perm_out,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * csr_permute_values — out[q] = values[perm[q]] for q < nnz (fp32 or bf16
+ * elements): moves a CSR's values into the order of a fixed transpose
+ * permutation (see csr_transpose), e.g. after each weight update.
+ */
+int csr_permute_values(int nnz, const int *perm, const void *values, usm_dtype dtype, void *out,
+                       void *stream);
+
+/*
  * usm_poll_status — synchronise `stream`, then return and clear the current
  * device's status word: USM_OK, or USM_ERR_TIMEOUT when a kernel's bounded
  * wait (on a TMA transfer) gave up and the kernel returned early (its output

@@ -65,6 +65,11 @@ def test_workspace_sizes(lib):
     assert lib.csr_sddmm_workspace_bytes(10, 10, 2048, 7, usm.USM_BF16) == 16 * 7 * 4
     assert lib.csr_sddmm_workspace_bytes(10, 10, 64, 7, usm.USM_BF16) == 0
     assert lib.csr_sddmm_workspace_bytes(10, 10, 0, 7, usm.USM_F32) == 0
+    # general SDDMM: transposed-Y region (K x ld, 256-byte aligned) + strip partials
+    assert lib.csr_sddmm_general_workspace_bytes(10, 10, 64, 7, usm.USM_F32, 1) == 0
+    assert lib.csr_sddmm_general_workspace_bytes(10, 10, 64, 7, usm.USM_F32, 0) == 2560  # 10 x 64 x 4
+    assert lib.csr_transpose_workspace_bytes(10, 10, 0) == 0
+    assert lib.csr_transpose_workspace_bytes(10, 10, 100) == 512 * 2 + 1024 + 512
 
 
 def spmm(lib, M=4, K=4, N=8, nnz=4, ro=A16, ci=A16, vals=A16, perm=None, B=A16, ldb=8, C=A16, ldc=8, dt=0):
@@ -121,6 +126,30 @@ def test_swizzle_rejects_bad_args_on_host(lib):
     assert lib.row_swizzle_build(4, 4, 0, A16, A16, None, 1 << 20, None) == -6
     assert lib.row_swizzle_build(4, 4, 0, A16, A16, A16, 8, None) == -6
     assert lib.row_swizzle_build(0, 4, 0, None, None, None, 0, None) == 0
+
+
+def test_next_rows_reject_bad_args_on_host(lib):
+    assert lib.csr_transpose(-1, 4, 4, A16, A16, A16, 0, A16, A16, A16, None, A16, 1 << 20, None) == -1
+    assert lib.csr_transpose(4, 0, 4, A16, A16, A16, 0, A16, A16, A16, None, A16, 1 << 20, None) == -1
+    assert lib.csr_transpose(4, 4, 4, A16, A16, A16, 0, A16, A16, None, None, A16, 1 << 20, None) == -1
+    assert lib.csr_transpose(4, 4, 4, A16, A16, A16, 0, A16, A16, A16, None, None, 0, None) == -6
+    assert lib.csr_transpose(4, 4, 4, A16, A16, A16, 0, A16, A16, A16, None, A16 + 16, 1 << 20, None) == -2
+    assert lib.csr_permute_values(-1, A16, A16, 0, A16, None) == -1
+    assert lib.csr_permute_values(5, None, A16, 0, A16, None) == -1
+    assert lib.csr_permute_values(0, None, None, 0, None, None) == 0
+    g = lambda **k: lib.csr_sddmm_general(*[k.get(n, v) for n, v in [
+        ("M", 4), ("K", 4), ("D", 8), ("nnz", 4), ("ro", A16), ("ci", A16), ("vals", None), ("perm", None),
+        ("X", A16), ("ldx", 8), ("Y", A16), ("ldy", 8), ("ytr", 1), ("out", A16), ("it", 0), ("ot", 0),
+        ("ws", None), ("wsb", 0), ("st", None)]])
+    assert g(ytr=2) == -1
+    assert g(ytr=0, ldy=3) == -1            # D x K operand needs ldy >= K
+    assert g(ytr=0) == -6                   # transposed copy of Y needs workspace
+    assert g(X=ODD) == -2
+    assert g(M=0) == 0
+    assert lib.csr_row_softmax(-1, 4, A16, A16, A16, 0, None) == -1
+    assert lib.csr_row_softmax(4, 4, A16, A16, A16, 3, None) == -1
+    assert lib.csr_row_softmax(4, 4, None, A16, A16, 0, None) == -1
+    assert lib.csr_row_softmax(0, 4, None, None, None, 0, None) == 0
 
 
 def test_selftest_rejects_bad_limit(lib):

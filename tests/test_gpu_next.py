@@ -1,0 +1,192 @@
+"""The next rows of the path, against the oracle through the C ABI:
+CSR transpose and the input-gradient SpMM (bit-exact structure), the
+general SDDMM (scaling and operand orientation), the row softmax, the
+sparse-attention chain with softmax, and the sparse layer's training step
+(forward SpMM, weight-gradient SDDMM, input-gradient SpMM on Aᵀ)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from parity_util import TOL, assert_within, dev, host, oracle_sddmm, oracle_spmm, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def csr_dev(csr):
+    return dev(csr.row_offsets), dev(csr.col_indices), dev(csr.values, csr.dtype)
+
+
+# ---------------------------------------------------------------------------
+# f1: CSR transpose (bit-exact) and the input gradient
+# ---------------------------------------------------------------------------
+TRANSPOSE_CASES = [
+    ("ragged", lambda dt: W.random_csr(1, 700, 300, 0.1, dtype=dt)),
+    ("empty_rows_and_cols", lambda dt: W.random_csr(2, 500, 5000, 0.0, dtype=dt,
+                                                    lengths=np.r_[np.zeros(250, int), np.full(250, 7)])),
+    ("one_row", lambda dt: W.random_csr(3, 1, 1000, 0.5, dtype=dt)),
+    ("one_col", lambda dt: W.random_csr(4, 1000, 1, 0.5, dtype=dt)),
+    ("dense", lambda dt: W.random_csr(5, 64, 64, 1.0, dtype=dt)),
+    ("no_nonzeros", lambda dt: W.random_csr(6, 100, 50, 0.0, dtype=dt)),
+    ("multi_tile", lambda dt: W.random_csr(7, 3000, 2000, 0.05, dtype=dt)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("name,make", TRANSPOSE_CASES, ids=[c[0] for c in TRANSPOSE_CASES])
+def test_transpose_bit_exact(usm, dtype, name, make):
+    csr = make(dtype)
+    ro, ci, vals = csr_dev(csr)
+    ro_t, ci_t, v_t, perm = usm.csr_transpose(ro, ci, vals, csr.K, with_perm=True)
+    w_ro, w_ci, w_v = oracle.csr_transpose(csr.M, csr.K, csr.row_offsets, csr.col_indices,
+                                           oracle.widen(csr.values, dtype))
+    assert np.array_equal(host(ro_t), w_ro)
+    assert np.array_equal(host(ci_t), w_ci)
+    assert np.array_equal(oracle.widen(host(v_t), dtype), w_v)
+    assert np.array_equal(host(v_t), csr.values[host(perm)])
+
+
+def test_transpose_full_configs(usm):
+    for csr in [W.ffn(4096, 1024, 70, "f32", with_spmm=False, with_sddmm=False).csr, W.lstm(50).csr,
+                W.attention().csr]:
+        ro, ci, vals = csr_dev(csr)
+        ro_t, ci_t, v_t = usm.csr_transpose(ro, ci, vals, csr.K)
+        w_ro, w_ci, w_v = oracle.csr_transpose(csr.M, csr.K, csr.row_offsets, csr.col_indices,
+                                               oracle.widen(csr.values, csr.dtype))
+        assert np.array_equal(host(ro_t), w_ro)
+        assert np.array_equal(host(ci_t), w_ci)
+        assert np.array_equal(oracle.widen(host(v_t), csr.dtype), w_v)
+
+
+def test_permute_values_follows_new_weights(usm):
+    csr = W.random_csr(8, 900, 600, 0.08)
+    ro, ci, vals = csr_dev(csr)
+    _, _, _, perm = usm.csr_transpose(ro, ci, vals, csr.K, with_perm=True)
+    new_vals = np.random.default_rng(9).standard_normal(csr.nnz).astype(np.float32)
+    got = host(usm.csr_permute_values(perm, dev(new_vals)))
+    _, _, want = oracle.csr_transpose(csr.M, csr.K, csr.row_offsets, csr.col_indices, new_vals.astype(np.float64))
+    assert np.array_equal(got.astype(np.float64), want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_input_gradient_spmm_on_transpose(usm, dtype):
+    M, K, N = 1500, 700, 136
+    csr = W.random_csr(10, M, K, 0.1, dtype=dtype)
+    dC = W.dense(np.random.default_rng(11), M, N, 1.0, dtype)
+    ro, ci, vals = csr_dev(csr)
+    ro_t, ci_t, v_t = usm.csr_transpose(ro, ci, vals, K)
+    dB = host(usm.spmm(ro_t, ci_t, v_t, dev(dC, dtype), K=M, row_swizzle=usm.row_swizzle(ro_t, M)))
+    t_ro, t_ci, t_v = oracle.csr_transpose(M, K, csr.row_offsets, csr.col_indices, oracle.widen(csr.values, dtype))
+    dCw = oracle.widen(dC, dtype)
+    ref = oracle.spmm(K, M, t_ro, t_ci, t_v, dCw)
+    S = oracle.spmm_error_scale(K, M, t_ro, t_ci, t_v, dCw)
+    assert_within(dB, ref, S, TOL[dtype], "input gradient")
+
+
+# ---------------------------------------------------------------------------
+# f2: general SDDMM
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("scale", [False, True])
+@pytest.mark.parametrize("ytr", [True, False])
+@pytest.mark.parametrize("M,K,D", [(300, 200, 64), (257, 333, 300), (40, 1000, 129)])
+def test_sddmm_general(usm, dtype, scale, ytr, M, K, D):
+    csr = W.random_csr([M, K, D, 12], M, K, 0.15, dtype=dtype)
+    rng = np.random.default_rng([M, K, D, 13])
+    X = W.dense(rng, M, D, 1.0, dtype)
+    Y = W.dense(rng, K, D, 1.0, dtype)
+    Yarg = Y if ytr else np.ascontiguousarray(Y.T)
+    ro, ci, vals = csr_dev(csr)
+    out = host(usm.sddmm_general(ro, ci, dev(X, dtype), dev(Yarg, dtype), values=vals if scale else None,
+                                 y_transposed=ytr))
+    a = oracle.widen(csr.values, dtype)
+    ref = oracle.sddmm_general(M, K, csr.row_offsets, csr.col_indices, a, scale, oracle.widen(X, dtype),
+                               oracle.widen(Yarg, dtype), ytr)
+    S = oracle.sddmm_error_scale(M, K, csr.row_offsets, csr.col_indices, oracle.widen(X, dtype),
+                                 oracle.widen(Y, dtype)) * (np.abs(a) if scale else 1.0)
+    assert_within(out, ref, S, TOL[dtype], f"general sddmm scale={scale} ytr={ytr}")
+
+
+def test_sddmm_general_matches_specialised_form(usm):
+    csr = W.random_csr(14, 500, 400, 0.1)
+    rng = np.random.default_rng(15)
+    X, Y = W.dense(rng, 500, 200), W.dense(rng, 400, 200)
+    ro, ci, _ = csr_dev(csr)
+    a = host(usm.sddmm(ro, ci, dev(X), dev(Y)))
+    b = host(usm.sddmm_general(ro, ci, dev(X), dev(Y)))
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# f4: row softmax and the attention chain with it
+# ---------------------------------------------------------------------------
+def test_row_softmax(usm):
+    import torch
+    lengths = np.r_[np.zeros(20, int), np.ones(20, int), np.arange(2, 300), [4096, 1000]]
+    csr = W.random_csr(16, lengths.size, 5000, 0.0, lengths=lengths)
+    s = (np.random.default_rng(17).standard_normal(csr.nnz) * 3).astype(np.float32)
+    ro = dev(csr.row_offsets)
+    p32 = host(usm.row_softmax(ro, dev(s)))
+    ref = oracle.csr_softmax(csr.row_offsets, s.astype(np.float64))
+    # ≤ n/32 + 8 roundings per output with n ≤ 4096: 136 u < 1e-5 relative
+    assert np.all(np.abs(p32 - ref) <= 1e-5 * ref)
+    p16 = host(usm.row_softmax(ro, dev(s), out_dtype=torch.bfloat16))
+    want = oracle.round_to_bf16(ref)
+    assert np.all(np.abs(p16.astype(np.int64) - want.astype(np.int64)) <= 1)
+    assert np.mean(p16 == want) > 0.99
+
+
+@pytest.mark.slow
+def test_attention_chain_with_softmax(usm):
+    import torch
+    p = W.attention()
+    csr = p.csr
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    perm = usm.row_swizzle(ro, csr.K, seg_rows=p.meta["seq"])
+    scores = usm.sddmm(ro, ci, dev(p.X, "bf16"), dev(p.Y, "bf16"), row_swizzle=perm)
+    probs = usm.row_softmax(ro, scores, out_dtype=torch.bfloat16)
+    O = host(usm.spmm(ro, ci, probs, dev(p.V, "bf16"), K=csr.K, row_swizzle=perm))
+    rows = sample_rows(csr.M, 128, 120, host(perm))
+    sub_ro, sub_ci, pos = oracle.select_rows(csr.row_offsets, csr.col_indices, rows)
+    Xw = oracle.widen(p.X, "bf16")[rows]
+    s64 = oracle.sddmm(rows.size, csr.K, sub_ro, sub_ci, Xw, oracle.widen(p.Y, "bf16"))
+    p16 = oracle.round_to_bf16(oracle.csr_softmax(sub_ro, s64))
+    got16 = host(probs)[pos]
+    assert np.all(np.abs(got16.astype(np.int64) - p16.astype(np.int64)) <= 1)
+    pw, Vw = oracle.widen(p16, "bf16"), oracle.widen(p.V, "bf16")
+    ref = oracle.spmm(rows.size, csr.K, sub_ro, sub_ci, pw, Vw)
+    S = oracle.spmm_error_scale(rows.size, csr.K, sub_ro, sub_ci, pw, Vw)
+    assert_within(O[rows], ref, S, TOL["bf16"], "attention with softmax")
+
+
+# ---------------------------------------------------------------------------
+# f3: the sparse layer's training step (forward, weight and input gradients)
+# ---------------------------------------------------------------------------
+@pytest.mark.slow
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_training_step_chain(usm, dtype):
+    p = W.ffn(4096, 1024, 90, dtype)
+    csr = p.csr
+    M, K, N = csr.M, csr.K, p.meta["N"]
+    dC = W.dense(np.random.default_rng(18), M, N, 1.0, dtype)
+    ro, ci, vals = csr_dev(csr)
+    perm = usm.row_swizzle(ro, K)
+    ro_t, ci_t, v_t, tperm = usm.csr_transpose(ro, ci, vals, K, with_perm=True)
+    perm_t = usm.row_swizzle(ro_t, M)
+    B, dCd = dev(p.B, dtype), dev(dC, dtype)
+    C = usm.spmm(ro, ci, vals, B, K=K, row_swizzle=perm)                  # forward
+    dA = usm.sddmm(ro, ci, dCd, B, row_swizzle=perm)                        # weight gradient
+    v_t = usm.csr_permute_values(tperm, vals, out=v_t)                      # weights in Aᵀ order
+    dB = usm.spmm(ro_t, ci_t, v_t, dCd, K=M, row_swizzle=perm_t)           # input gradient
+    rows = sample_rows(M, 96, 19, host(perm))
+    ref, S = oracle_spmm(csr, p.B, dtype, rows)
+    assert_within(host(C)[rows], ref, S, TOL[dtype], "forward")
+    ref, S, pos = oracle_sddmm(csr, dC, p.B, dtype, rows)
+    assert_within(host(dA)[pos], ref, S, TOL[dtype], "weight gradient")
+    t_ro, t_ci, t_v = oracle.csr_transpose(M, K, csr.row_offsets, csr.col_indices, oracle.widen(csr.values, dtype))
+    rows_t = sample_rows(K, 96, 20)
+    s_ro, s_ci, s_pos = oracle.select_rows(t_ro, t_ci, rows_t)
+    dCw = oracle.widen(dC, dtype)
+    ref = oracle.spmm(rows_t.size, M, s_ro, s_ci, t_v[s_pos], dCw)
+    S = oracle.spmm_error_scale(rows_t.size, M, s_ro, s_ci, t_v[s_pos], dCw)
+    assert_within(host(dB)[rows_t], ref, S, TOL[dtype], "input gradient")

@@ -37,6 +37,13 @@ SIGNATURES = {
     "usm_status_string": (ctypes.c_char_p, [_i]),
     "usm_selftest_wait_timeout": (_i, [_ll, _vp]),
     "csr_sddmm_static_scratch": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _vp]),
+    "csr_transpose_workspace_bytes": (_sz, [_i, _i, _i]),
+    "csr_sddmm_general_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "csr_sddmm_general": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _vp, _i, _i, _vp, _sz,
+                               _vp]),
+    "csr_row_softmax": (_i, [_i, _i, _vp, _vp, _vp, _i, _vp]),
+    "csr_transpose": (_i, [_i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "csr_permute_values": (_i, [_i, _vp, _vp, _i, _vp, _vp]),
 }
 
 _lib = None
@@ -215,6 +222,87 @@ def sddmm(row_offsets, col_indices, X, Y, row_swizzle=None, out=None, out_dtype=
                          _ptr(X), _ld(X), _ptr(Y), _ld(Y), _ptr(out), in_code, out_code,
                          _ptr(workspace) if ws_bytes else None, ws_bytes, _stream(stream))
     _check("csr_sddmm", code)
+    return out
+
+
+def sddmm_general(row_offsets, col_indices, X, Y, values=None, y_transposed=True, row_swizzle=None, out=None,
+                  out_dtype=None, stream=None):
+    """out[p] = (values[p] if given) · X[r]·Yop[col_p]; Yop = Y (K×D) when
+    y_transposed, else Yᵀ with Y given D×K."""
+    torch = _torch()
+    lib = load()
+    _require(row_offsets, "row_offsets", (torch.int32,))
+    _require(col_indices, "col_indices", (torch.int32,))
+    _require(X, "X", (torch.float32, torch.bfloat16))
+    _require(Y, "Y", (X.dtype,))
+    if values is not None:
+        _require(values, "values", (X.dtype,))
+    M = row_offsets.numel() - 1
+    D = X.shape[1]
+    K = Y.shape[0] if y_transposed else Y.shape[1]
+    if (Y.shape[1] if y_transposed else Y.shape[0]) != D:
+        raise ValueError("X and Y disagree on D")
+    X = _tma_ready(X)
+    if y_transposed:
+        Y = _tma_ready(Y)
+    elif Y.stride(1) != 1:
+        Y = Y.contiguous()
+    nnz = col_indices.numel()
+    if out is None:
+        out = torch.empty(nnz, dtype=out_dtype if out_dtype is not None else torch.float32, device=X.device)
+    in_code = _dtype_code(X)
+    ws_bytes = lib.csr_sddmm_general_workspace_bytes(M, K, D, nnz, in_code, int(bool(y_transposed)))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=X.device)
+    code = lib.csr_sddmm_general(M, K, D, nnz, _ptr(row_offsets), _ptr(col_indices), _ptr(values),
+                                 _ptr(row_swizzle), _ptr(X), _ld(X), _ptr(Y), Y.stride(0), int(bool(y_transposed)),
+                                 _ptr(out), in_code, _dtype_code(out), _ptr(ws) if ws_bytes else None, ws_bytes,
+                                 _stream(stream))
+    _check("csr_sddmm_general", code)
+    return out
+
+
+def row_softmax(row_offsets, scores, out=None, out_dtype=None, stream=None):
+    """Softmax over the stored entries of each CSR row (fp32 scores in)."""
+    torch = _torch()
+    lib = load()
+    _require(row_offsets, "row_offsets", (torch.int32,))
+    _require(scores, "scores", (torch.float32,))
+    if out is None:
+        out = torch.empty_like(scores, dtype=out_dtype if out_dtype is not None else torch.float32)
+    code = lib.csr_row_softmax(row_offsets.numel() - 1, scores.numel(), _ptr(row_offsets), _ptr(scores), _ptr(out),
+                               _dtype_code(out), _stream(stream))
+    _check("csr_row_softmax", code)
+    return out
+
+
+def csr_transpose(row_offsets, col_indices, values, K: int, with_perm: bool = False, stream=None):
+    """Aᵀ in CSR: (row_offsets_t, col_indices_t, values_t[, perm])."""
+    torch = _torch()
+    lib = load()
+    _require(row_offsets, "row_offsets", (torch.int32,))
+    _require(col_indices, "col_indices", (torch.int32,))
+    M = row_offsets.numel() - 1
+    nnz = col_indices.numel()
+    dev = row_offsets.device
+    ro_t = torch.empty(K + 1, dtype=torch.int32, device=dev)
+    ci_t = torch.empty(nnz, dtype=torch.int32, device=dev)
+    v_t = torch.empty_like(values) if values is not None else None
+    perm = torch.empty(nnz, dtype=torch.int32, device=dev) if with_perm else None
+    code_dt = _dtype_code(values) if values is not None else USM_F32
+    ws_bytes = lib.csr_transpose_workspace_bytes(M, K, nnz)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    code = lib.csr_transpose(M, K, nnz, _ptr(row_offsets), _ptr(col_indices), _ptr(values), code_dt, _ptr(ro_t),
+                             _ptr(ci_t), _ptr(v_t), _ptr(perm), _ptr(ws), ws_bytes, _stream(stream))
+    _check("csr_transpose", code)
+    return (ro_t, ci_t, v_t, perm) if with_perm else (ro_t, ci_t, v_t)
+
+
+def csr_permute_values(perm, values, out=None, stream=None):
+    """out[q] = values[perm[q]]."""
+    lib = load()
+    out = out if out is not None else values.new_empty(perm.numel())
+    _check("csr_permute_values", lib.csr_permute_values(perm.numel(), _ptr(perm), _ptr(values), _dtype_code(values),
+                                                        _ptr(out), _stream(stream)))
     return out
 
 

@@ -166,6 +166,103 @@ int row_swizzle_build(int M, int K, int seg_rows, const int* row_offsets, int* s
                               as_stream(stream));
 }
 
+namespace {
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+// Leading dimension of the transposed Y the general SDDMM builds (16-byte rows).
+long long yt_ld(int D, bool bf16) {
+    const int per = bf16 ? 8 : 4;
+    return ((long long)D + per - 1) / per * per;
+}
+size_t general_yt_bytes(int K, int D, bool bf16, int y_transposed) {
+    if (y_transposed || K <= 0 || D <= 0) return 0;
+    return align256((size_t)K * (size_t)yt_ld(D, bf16) * (bf16 ? 2 : 4));
+}
+}  // namespace
+
+size_t csr_sddmm_general_workspace_bytes(int M, int K, int D, int nnz, usm_dtype in_dtype, int y_transposed) {
+    if (M <= 0 || K < 0 || D <= 0 || nnz <= 0) return 0;
+    const bool bf = in_dtype == USM_BF16;
+    return general_yt_bytes(K, D, bf, y_transposed) + sddmm_workspace_bytes(M, K, D, nnz, bf);
+}
+
+int csr_sddmm_general(int M, int K, int D, int nnz, const int* row_offsets, const int* col_indices,
+                      const void* values, const int* row_swizzle, const void* X, int ldx, const void* Y, int ldy,
+                      int y_transposed, void* out, usm_dtype in_dtype, usm_dtype out_dtype, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    if (M < 0 || K < 0 || D < 0 || nnz < 0) return USM_ERR_INVALID_ARG;
+    if ((in_dtype != USM_F32 && in_dtype != USM_BF16) || (out_dtype != USM_F32 && out_dtype != USM_BF16))
+        return USM_ERR_INVALID_ARG;
+    if (y_transposed != 0 && y_transposed != 1) return USM_ERR_INVALID_ARG;
+    if (M == 0 || nnz == 0) return USM_OK;
+    if (!out || !row_offsets || !col_indices) return USM_ERR_INVALID_ARG;
+    if (K == 0) return USM_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    if (D == 0) return launch_fill_out(out, nnz, out_dtype == USM_BF16, st);
+    const bool bf = in_dtype == USM_BF16;
+    const int es = bf ? 2 : 4;
+    if (!X || !Y || ldx < D) return USM_ERR_INVALID_ARG;
+    if (y_transposed ? ldy < D : ldy < K) return USM_ERR_INVALID_ARG;
+    if (!aligned16(X) || ((long long)ldx * es) % 16 != 0) return USM_ERR_ALIGNMENT;
+    if (y_transposed && (!aligned16(Y) || ((long long)ldy * es) % 16 != 0)) return USM_ERR_ALIGNMENT;
+    const size_t yt_bytes = general_yt_bytes(K, D, bf, y_transposed);
+    const size_t part_bytes = sddmm_workspace_bytes(M, K, D, nnz, bf);
+    const size_t need = yt_bytes + part_bytes;
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return USM_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return USM_ERR_ALIGNMENT;
+    int* status = status_word_for_current_device();
+    if (!status) return USM_ERR_CUDA;
+    const void* Yk = Y;
+    long long ldyk = ldy;
+    if (!y_transposed) {
+        ldyk = yt_ld(D, bf);
+        const int r = launch_dense_transpose(Y, ldy, D, K, bf, workspace, ldyk, st);
+        if (r != USM_OK) return r;
+        Yk = workspace;
+    }
+    if (ldyk > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
+    SddmmArgs a{M, K, D, nnz, row_offsets, col_indices, row_swizzle, X, ldx, out, 0,
+                out_dtype == USM_BF16 ? 1 : 0, 1, status, values, bf ? 1 : 0};
+    void* part = part_bytes ? static_cast<unsigned char*>(workspace) + yt_bytes : nullptr;
+    return launch_sddmm(a, Yk, (int)ldyk, bf, part, part_bytes, st);
+}
+
+int csr_row_softmax(int M, int nnz, const int* row_offsets, const float* scores, void* out, usm_dtype out_dtype,
+                    void* stream) {
+    if (M < 0 || nnz < 0) return USM_ERR_INVALID_ARG;
+    if (out_dtype != USM_F32 && out_dtype != USM_BF16) return USM_ERR_INVALID_ARG;
+    if (M == 0 || nnz == 0) return USM_OK;
+    if (!row_offsets || !scores || !out) return USM_ERR_INVALID_ARG;
+    return launch_row_softmax(M, nnz, row_offsets, scores, out, out_dtype == USM_BF16, as_stream(stream));
+}
+
+size_t csr_transpose_workspace_bytes(int M, int K, int nnz) {
+    if (M < 0 || K < 0 || nnz <= 0) return 0;
+    return transpose_workspace_bytes(M, K, nnz);
+}
+
+int csr_transpose(int M, int K, int nnz, const int* row_offsets, const int* col_indices, const void* values,
+                  usm_dtype dtype, int* row_offsets_t, int* col_indices_t, void* values_t, int* perm_out,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+    if (M < 0 || K < 0 || nnz < 0) return USM_ERR_INVALID_ARG;
+    if (dtype != USM_F32 && dtype != USM_BF16) return USM_ERR_INVALID_ARG;
+    if (!row_offsets_t) return USM_ERR_INVALID_ARG;
+    if (nnz > 0 && (K == 0 || !row_offsets || !col_indices || !col_indices_t)) return USM_ERR_INVALID_ARG;
+    if ((values == nullptr) != (values_t == nullptr)) return USM_ERR_INVALID_ARG;
+    const size_t need = transpose_workspace_bytes(M, K, nnz);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return USM_ERR_WORKSPACE;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return USM_ERR_ALIGNMENT;
+    return launch_csr_transpose(M, K, nnz, row_offsets, col_indices, values, dtype == USM_BF16, row_offsets_t,
+                                col_indices_t, values_t, perm_out, workspace, workspace_bytes, as_stream(stream));
+}
+
+int csr_permute_values(int nnz, const int* perm, const void* values, usm_dtype dtype, void* out, void* stream) {
+    if (nnz < 0) return USM_ERR_INVALID_ARG;
+    if (dtype != USM_F32 && dtype != USM_BF16) return USM_ERR_INVALID_ARG;
+    if (nnz == 0) return USM_OK;
+    if (!perm || !values || !out) return USM_ERR_INVALID_ARG;
+    return launch_permute_values(nnz, perm, values, dtype == USM_BF16, out, as_stream(stream));
+}
+
 int usm_poll_status(void* stream) {
     cudaStream_t st = as_stream(stream);
     if (cudaStreamSynchronize(st) != cudaSuccess) return USM_ERR_CUDA;

@@ -33,6 +33,8 @@ struct SddmmArgs {
     int out_bf16;        // final output element type is bf16
     int rows_per_warp;
     int* status;
+    const void* scale;   // null, or the mask's values: out[p] is multiplied by scale[p]
+    int scale_bf16;      // scale elements are bf16 (else fp32)
 };
 
 // Device status word of the current device (null if it cannot be resolved).
@@ -54,10 +56,39 @@ size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16);
 int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* workspace,
                  size_t workspace_bytes, cudaStream_t stream);
 int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream);
+// Dense transpose: dst (cols × rows, leading dimension ldd) = srcᵀ (rows × cols, lds).
+int launch_dense_transpose(const void* src, long long lds, int rows, int cols, bool bf16, void* dst,
+                           long long ldd, cudaStream_t stream);
+int launch_row_softmax(int M, int nnz, const int* row_offsets, const float* scores, void* out, bool out_bf16,
+                       cudaStream_t stream);
+
+// Stable LSD radix sort of item ids 0..n-1 by a key (8 bits per pass).
+enum class SortKey { RowSwizzle, Column };
+struct SortSpec {
+    SortKey kind;
+    const int* row_offsets;  // RowSwizzle: key = (segment, K - row length)
+    const int* col_indices;  // Column: key = col_indices[item]
+    long long n;             // number of items
+    int K;
+    int seg_rows;
+    int len_bits;
+};
+size_t stable_sort_workspace_bytes(long long n);
+int launch_stable_sort(const SortSpec& spec, int key_bits, int* out, void* ws, size_t ws_bytes,
+                       cudaStream_t stream);
+int bits_for(long long v);
+int launch_exclusive_scan(int* data, long long n, cudaStream_t stream);  // in place, one block
 
 size_t swizzle_workspace_bytes(int M, int K);
 int launch_row_swizzle(int M, int K, int seg_rows, const int* row_offsets, int* perm,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+size_t transpose_workspace_bytes(int M, int K, int nnz);
+int launch_csr_transpose(int M, int K, int nnz, const int* row_offsets, const int* col_indices,
+                         const void* values, bool bf16, int* ro_t, int* ci_t, void* values_t, int* perm_out,
+                         void* ws, size_t ws_bytes, cudaStream_t stream);
+int launch_permute_values(int nnz, const int* perm, const void* values, bool bf16, void* out,
+                          cudaStream_t stream);
 
 int launch_wait_timeout_selftest(long long limit_ns, int* status, cudaStream_t stream);
 

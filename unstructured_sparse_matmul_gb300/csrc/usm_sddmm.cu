@@ -49,6 +49,13 @@ struct SddmmCfg {
     static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
 };
 
+// Scaling by the mask's value at nonzero p (general SDDMM), 1 otherwise.
+__device__ __forceinline__ float scale_at(const void* scale, int scale_bf16, long long p) {
+    if (!scale) return 1.f;
+    if (scale_bf16) return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(scale) + p) << 16);
+    return __ldg(reinterpret_cast<const float*>(scale) + p);
+}
+
 __device__ __forceinline__ int window_col(const SddmmArgs& a, int pos, int end, int lane) {
     const int p = pos + lane;
     return p < end ? __ldg(a.col_indices + p) : INT_MAX;
@@ -288,10 +295,11 @@ __global__ void __launch_bounds__(W * 32, MINB)
                     if (e < n) {
                         const long long p = (long long)rc + e;
                         if (single_strip) {
+                            const float v = a.scale ? part[0] * scale_at(a.scale, a.scale_bf16, p) : part[0];
                             if (a.out_bf16)
-                                reinterpret_cast<uint16_t*>(a.out)[p] = f32_to_bf16_rne(part[0]);
+                                reinterpret_cast<uint16_t*>(a.out)[p] = f32_to_bf16_rne(v);
                             else
-                                reinterpret_cast<float*>(a.out)[p] = part[0];
+                                reinterpret_cast<float*>(a.out)[p] = v;
                         } else {
                             reinterpret_cast<float*>(a.out)[(long long)strip * a.out_stride + p] = part[0];
                         }
@@ -325,13 +333,15 @@ __global__ void __launch_bounds__(W * 32, MINB)
     }
 }
 
-// out[p] = Σ_s partial[s][p], strips added in increasing order.
+// out[p] = Σ_s partial[s][p] (strips added in increasing order), times the
+// mask's value when scaling.
 __global__ void sddmm_strip_sum_kernel(const float* __restrict__ part, long long nnz, int nstrips,
-                                       void* out, int out_bf16) {
+                                       void* out, int out_bf16, const void* scale, int scale_bf16) {
     for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < nnz;
          p += (long long)gridDim.x * blockDim.x) {
         float s = part[p];
         for (int k = 1; k < nstrips; ++k) s += part[(long long)k * nnz + p];
+        if (scale) s *= scale_at(scale, scale_bf16, p);
         if (out_bf16)
             reinterpret_cast<uint16_t*>(out)[p] = f32_to_bf16_rne(s);
         else
@@ -386,7 +396,8 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
         long long blocks = ((long long)a.nnz + 255) / 256;
         if (blocks > 8 * sms) blocks = 8 * sms;
         sddmm_strip_sum_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz,
-                                                                nstrips, final_out, a.out_bf16);
+                                                                nstrips, final_out, a.out_bf16, a.scale,
+                                                                a.scale_bf16);
         if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
     }
     return USM_OK;
@@ -405,6 +416,39 @@ size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16) {
     const int dt = strip_width(D, bf16);
     const long long nstrips = (D + dt - 1) / dt;
     return nstrips > 1 ? (size_t)nstrips * (size_t)nnz * sizeof(float) : 0;
+}
+
+namespace {
+// 32×32 tiles through shared memory (padded against bank conflicts).
+template <typename T>
+__global__ void dense_transpose_kernel(const T* __restrict__ src, long long lds, int rows, int cols,
+                                       T* __restrict__ dst, long long ldd) {
+    __shared__ T tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[i][threadIdx.x] = src[(long long)r * lds + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, r = r0 + threadIdx.x;
+        if (r < rows && c < cols) dst[(long long)c * ldd + r] = tile[threadIdx.x][i];
+    }
+}
+}  // namespace
+
+int launch_dense_transpose(const void* src, long long lds, int rows, int cols, bool bf16, void* dst,
+                           long long ldd, cudaStream_t stream) {
+    if ((long long)rows * cols == 0) return USM_OK;
+    const dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
+    if (grid.y > 65535u) return USM_ERR_UNSUPPORTED;
+    if (bf16)
+        dense_transpose_kernel<uint16_t><<<grid, block, 0, stream>>>(static_cast<const uint16_t*>(src), lds, rows, cols,
+                                                                     static_cast<uint16_t*>(dst), ldd);
+    else
+        dense_transpose_kernel<float><<<grid, block, 0, stream>>>(static_cast<const float*>(src), lds, rows, cols,
+                                                                  static_cast<float*>(dst), ldd);
+    return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
 }
 
 int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream) {
