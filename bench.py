@@ -58,9 +58,19 @@ def tag_of(dtype, M, K, s):
     return f"{dtype}_{M}x{K}_s{s}"
 
 
-def problems(only=None):
-    """Problems of one step (each used by one SpMM and one SDDMM launch).
-    `only` keeps the problems whose tag contains that substring."""
+WORKLOADS = {
+    "ffn": "the hot path: SpMM forward + SDDMM weight-gradient per FFN problem (the bench line)",
+    "ffn_train": "the sparse layer's training step per FFN problem: forward SpMM, weight-gradient SDDMM "
+                 "(X = dC, Y = B), weights permuted into Aᵀ order, input-gradient SpMM on Aᵀ",
+    "attention": "sparse attention, 8 heads x 4096, bf16: SDDMM scores, row softmax, SpMM with V",
+}
+
+
+def problems(only=None, workload="ffn"):
+    """Problems of one step.  `only` keeps the problems whose tag contains
+    that substring."""
+    if workload == "attention":
+        return [W.attention()]
     out = []
     for dtype in ("f32", "bf16"):
         for (M, K) in W.FFN_SHAPES:
@@ -71,24 +81,43 @@ def problems(only=None):
     return out
 
 
-def ops_of(only):
-    """--only spmm:<tag> / sddmm:<tag> restricts the operation too."""
+def ops_of(only, workload="ffn"):
+    """Launches per problem; --only spmm:<tag> / sddmm:<tag> restricts the
+    operation too."""
     if only and ":" in only:
         return (only.split(":")[0],)
+    if workload == "ffn_train":
+        return ("spmm", "sddmm_w", "permute", "spmm_t")
+    if workload == "attention":
+        return ("sddmm", "softmax", "spmm")
     return ("spmm", "sddmm")
 
 
+def width_of(p):
+    return p.meta.get("N", N_FFN)
+
+
 def flops_of(p, op):
-    return 2.0 * p.csr.nnz * N_FFN
+    """Useful flops: 2·nnz·N for every product; the permutation and the
+    softmax are not counted (their time is)."""
+    if op in ("permute", "softmax"):
+        return 0.0
+    return 2.0 * p.csr.nnz * width_of(p)
 
 
 def alg_bytes(p, op):
     """Bytes the operation must move at minimum (each operand once)."""
     es = 2 if p.dtype == "bf16" else 4
-    M, K, nnz = p.csr.M, p.csr.K, p.csr.nnz
+    M, K, nnz, N = p.csr.M, p.csr.K, p.csr.nnz, width_of(p)
     if op == "spmm":
-        return nnz * (es + 4) + 4 * (M + 1) + K * N_FFN * es + 4 * M * N_FFN
-    return nnz * (4 + 4) + 4 * (M + 1) + (M + K) * N_FFN * es
+        return nnz * (es + 4) + 4 * (M + 1) + K * N * es + 4 * M * N
+    if op == "spmm_t":  # Aᵀ (K x M) · dC (M x N) -> K x N
+        return nnz * (es + 4) + 4 * (K + 1) + M * N * es + 4 * K * N
+    if op == "permute":
+        return nnz * (4 + 2 * es)
+    if op == "softmax":
+        return nnz * (4 + es) + 4 * (M + 1)
+    return nnz * (4 + 4) + 4 * (M + 1) + (M + K) * N * es  # SDDMM variants, fp32 out
 
 
 # ---------------------------------------------------------------------------
@@ -155,24 +184,41 @@ def run_ours(args, rank, world, local_rank):
             return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
         return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
 
-    probs = problems(args.only)
+    wl = args.workload
+    probs = problems(args.only, wl)
     if not probs:
         raise SystemExit(f"--only {args.only!r} matches no launch")
+    lib = usm.load()
     items = []
     for p in probs:
         csr = p.csr
-        d = {
-            "p": p,
-            "ro": to_dev(csr.row_offsets, "i32"), "ci": to_dev(csr.col_indices, "i32"),
-            "vals": to_dev(csr.values, p.dtype),
-            "B": to_dev(p.B, p.dtype), "X": to_dev(p.X, p.dtype), "Y": to_dev(p.Y, p.dtype),
-        }
-        d["C"] = torch.empty((csr.M, N_FFN), dtype=torch.float32, device=dev)
-        d["out"] = torch.empty(csr.nnz, dtype=torch.float32, device=dev)
-        lib = usm.load()
-        ws_bytes = lib.csr_sddmm_workspace_bytes(csr.M, csr.K, N_FFN, csr.nnz, 1 if p.dtype == "bf16" else 0)
+        N = width_of(p)
+        bf = p.dtype == "bf16"
+        d = {"p": p, "ro": to_dev(csr.row_offsets, "i32"), "ci": to_dev(csr.col_indices, "i32")}
+        seg = p.meta.get("seq", 0) if wl == "attention" else 0
+        d["perm"] = usm.row_swizzle(d["ro"], csr.K, seg_rows=seg)
+        if wl == "attention":
+            d["X"], d["Y"], d["V"] = to_dev(p.X, "bf16"), to_dev(p.Y, "bf16"), to_dev(p.V, "bf16")
+            d["S"] = torch.empty(csr.nnz, dtype=torch.float32, device=dev)
+            d["P"] = torch.empty(csr.nnz, dtype=torch.bfloat16, device=dev)
+            d["C"] = torch.empty((csr.M, N), dtype=torch.float32, device=dev)
+            ws_bytes = 0
+        else:
+            d["vals"] = to_dev(csr.values, p.dtype)
+            d["B"] = to_dev(p.B, p.dtype)
+            d["C"] = torch.empty((csr.M, N), dtype=torch.float32, device=dev)
+            d["out"] = torch.empty(csr.nnz, dtype=torch.float32, device=dev)
+            if wl == "ffn_train":
+                d["dC"] = to_dev(W.dense(W.rng_for(9, p.meta["sparsity"], 6), csr.M, N, 1.0, p.dtype), p.dtype)
+                d["ro_t"], d["ci_t"], d["v_t"], d["tperm"] = usm.csr_transpose(d["ro"], d["ci"], d["vals"], csr.K,
+                                                                               with_perm=True)
+                d["perm_t"] = usm.row_swizzle(d["ro_t"], csr.M)
+                d["dB"] = torch.empty((csr.K, N), dtype=torch.float32, device=dev)
+            else:
+                d["X"], d["Y"] = to_dev(p.X, p.dtype), to_dev(p.Y, p.dtype)
+            ws_bytes = lib.csr_sddmm_workspace_bytes(csr.M, csr.K, N, csr.nnz, 1 if bf else 0)
         d["ws"] = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-        d["perm"] = usm.row_swizzle(d["ro"], csr.K)
+        d["nk_sddmm"] = 2 if ws_bytes > 0 else 1
         items.append(d)
     torch.cuda.synchronize()
 
@@ -180,23 +226,30 @@ def run_ours(args, rank, world, local_rank):
     launches = []
     for d in items:
         p = d["p"]
-        tag = tag_of(p.dtype, p.csr.M, p.csr.K, p.meta["sparsity"])
-        for op in ops_of(args.only):
+        tag = "bf16_8x4096_h64" if wl == "attention" else tag_of(p.dtype, p.csr.M, p.csr.K, p.meta["sparsity"])
+        for op in ops_of(args.only, wl):
             launches.append((f"{op}_{tag}", op, d))
-    kernels_per_launch = {}
-    for label, op, d in launches:
-        p = d["p"]
-        n = 1
-        if op == "sddmm":
-            code = 1 if p.dtype == "bf16" else 0
-            n += 1 if lib.csr_sddmm_workspace_bytes(p.csr.M, p.csr.K, N_FFN, p.csr.nnz, code) > 0 else 0
-        kernels_per_launch[label] = n
+    kernels_per_launch = {label: (d["nk_sddmm"] if op.startswith("sddmm") else 1) for label, op, d in launches}
 
     def run_one(op, d):
-        if op == "spmm":
-            usm.spmm(d["ro"], d["ci"], d["vals"], d["B"], K=d["p"].csr.K, row_swizzle=d["perm"], out=d["C"])
-        else:
+        K = d["p"].csr.K
+        if wl == "attention":
+            if op == "sddmm":
+                usm.sddmm(d["ro"], d["ci"], d["X"], d["Y"], row_swizzle=d["perm"], out=d["S"])
+            elif op == "softmax":
+                usm.row_softmax(d["ro"], d["S"], out=d["P"])
+            else:
+                usm.spmm(d["ro"], d["ci"], d["P"], d["V"], K=K, row_swizzle=d["perm"], out=d["C"])
+        elif op == "spmm":
+            usm.spmm(d["ro"], d["ci"], d["vals"], d["B"], K=K, row_swizzle=d["perm"], out=d["C"])
+        elif op == "sddmm":
             usm.sddmm(d["ro"], d["ci"], d["X"], d["Y"], row_swizzle=d["perm"], out=d["out"], workspace=d["ws"])
+        elif op == "sddmm_w":
+            usm.sddmm(d["ro"], d["ci"], d["dC"], d["B"], row_swizzle=d["perm"], out=d["out"], workspace=d["ws"])
+        elif op == "permute":
+            usm.csr_permute_values(d["tperm"], d["vals"], out=d["v_t"])
+        elif op == "spmm_t":
+            usm.spmm(d["ro_t"], d["ci_t"], d["v_t"], d["dC"], K=d["p"].csr.M, row_swizzle=d["perm_t"], out=d["dB"])
 
     def step(events=None):
         for i, (label, op, d) in enumerate(launches):
@@ -258,7 +311,7 @@ def run_ours(args, rank, world, local_rank):
     traffic = recorded_traffic(dom_label)
 
     # End to end through the public API with host buffers.
-    e2e = run_e2e(args, usm, torch, dev, launches, step_flops) if not args.no_e2e else None
+    e2e = run_e2e(args, usm, torch, dev, launches, step_flops) if not args.no_e2e and wl == "ffn" else None
 
     result = {
         "metric": "SpMM/SDDMM useful GFLOP/s (2·nnz·N), HBM GB/s, % of roofline on 1 GB300",
@@ -273,7 +326,8 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded, shaped like the pages' Transformer-FFN weights)",
-        "config": {"workload": WORKLOAD if not args.only else f"{WORKLOAD} [only {args.only}]",
+        "config": {"workload": (WORKLOAD if wl == "ffn" else f"{wl}: {WORKLOADS[wl]}")
+                   + (f" [only {args.only}]" if args.only else ""),
                    "launches_per_step": len(launches),
                    "l2": "inputs larger than L2: each step touches ~1.1 GB of operands",
                    "swizzle": "row swizzle built once per pattern before timing",
@@ -290,7 +344,7 @@ def run_ours(args, rank, world, local_rank):
     }
     if e2e is not None:
         result["e2e"] = e2e
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl == "ffn":
         result["cpu_baseline"] = cpu_baseline(args.cpu_sample, args.only)
     return result
 
@@ -440,6 +494,8 @@ def main():
                     help="row fraction of each launch per step of the --impl reference arm")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="ffn", choices=sorted(WORKLOADS),
+                    help="ffn (default, the bench line) or a measurement of the next rows")
     ap.add_argument("--only", default=None,
                     help="restrict to launches whose tag contains this (e.g. spmm:f32_4096x1024_s70); "
                          "for profiling a single kernel, not a bench line")
