@@ -45,13 +45,16 @@
 namespace usm {
 namespace {
 
-template <bool BF, int L, int R, int W, int KC, int NS>
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS>
 struct SpmmCfg {
     static constexpr int ES = BF ? 2 : 4;          // element bytes
-    static constexpr int NT = L * 4;               // output columns per CTA (4 per lane)
+    static constexpr int NT = L * VEC;             // output columns per CTA (VEC per lane)
     static constexpr int G = 32 / L;               // lane groups (nonzeros per warp step)
-    static constexpr int LANE_BYTES = 4 * ES;      // B bytes per lane per step
+    static constexpr int LANE_BYTES = VEC * ES;    // B bytes per lane per step
+    static constexpr int NCH = LANE_BYTES / 16;    // 16-byte loads per lane per step (0: one 8-byte load)
+    static constexpr int EPC = 16 / ES;            // elements per 16-byte chunk
     static constexpr int PITCH = L * LANE_BYTES;   // bytes per staged B row
+    static constexpr int NW = LANE_BYTES / 4;      // 32-bit words per lane per step
     static constexpr int STAGE = KC * PITCH;
     static constexpr int MT = R * W;
     static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
@@ -63,7 +66,19 @@ struct SpmmCfg {
     static_assert(32 % L == 0, "L must divide the warp");
     static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
     static_assert(!BF || STAGE / 8 < 65536, "bf16 entry offsets are 16-bit multiples of 8 bytes");
+    static_assert(LANE_BYTES == 8 || LANE_BYTES == 16 || LANE_BYTES == 32, "8, 16 or 32 bytes per lane");
+    static_assert(NT <= 256, "TMA box width");
 };
+
+// Output column (within the strip) of element v of lane l.  8-byte lanes own
+// VEC contiguous columns; wider lanes own one 16-byte chunk per L·16-byte
+// slice of the staged row, so every warp-wide load reads contiguous bytes.
+template <int L, int VEC, int ES>
+__device__ __forceinline__ int lane_col(int l, int v) {
+    constexpr int EPC = 16 / ES;
+    if constexpr (VEC * ES == 8) return l * VEC + v;
+    return (v / EPC) * L * EPC + l * EPC + (v % EPC);
+}
 
 // Window of 32 consecutive nonzeros of a row starting at `pos`: lane i gets
 // nonzero pos+i (column INT_MAX past the row end).
@@ -83,10 +98,11 @@ __device__ __forceinline__ void load_window(const SpmmArgs& a, int pos, int end,
     }
 }
 
-template <bool BF, int L, int R, int W, int KC, int NS>
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS>
 __global__ void __launch_bounds__(W * 32, 2)
     spmm_kernel(const __grid_constant__ CUtensorMap tmB, const SpmmArgs a) {
-    using C_ = SpmmCfg<BF, L, R, W, KC, NS>;
+    using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
+    constexpr int NCH = C_::NCH, NW = C_::NW;
     constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, ENTRY = C_::ENTRY;
 
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -166,11 +182,11 @@ __global__ void __launch_bounds__(W * 32, 2)
         if (NS > 1 && nchunks > 1) issue(1);
     }
 
-    float acc[R][4];
+    float acc[R][VEC];
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int v = 0; v < 4; ++v) acc[i][v] = 0.f;
+        for (int v = 0; v < VEC; ++v) acc[i][v] = 0.f;
 
     int cur = my_start;  // lane i: cursor of row slot i
     int pcol;
@@ -186,7 +202,7 @@ __global__ void __launch_bounds__(W * 32, 2)
         const int k0 = (c_lo + j) * KC;
         const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs);
         if (!ok) kr[2] = 1;
-        const uint32_t stage = smem_addr(stages + s * STAGE) + l * C_::LANE_BYTES;
+        const uint32_t stage = smem_addr(stages + s * STAGE) + l * (NCH ? 16 : 8);
         if (ok) {
 #pragma unroll
             for (int i = 0; i < R; ++i) {
@@ -197,8 +213,10 @@ __global__ void __launch_bounds__(W * 32, 2)
                 if (i + 1 < R)
                     load_window<BF>(a, __shfl_sync(kFullMask, cur, i + 1),
                                     __shfl_sync(kFullMask, my_end, i + 1), lane, pcol, pval);
-                float c4[4] = {0.f, 0.f, 0.f, 0.f};  // fp32: this window's partial sums (≤ 32 terms)
-                float cc[4] = {0.f, 0.f, 0.f, 0.f};  // fp32: this chunk segment's windows
+                float c4[BF ? 1 : VEC];  // fp32: this window's partial sums (≤ 32 terms)
+                float cc[BF ? 1 : VEC];  // fp32: this chunk segment's windows
+#pragma unroll
+                for (int v = 0; v < (BF ? 1 : VEC); ++v) c4[v] = cc[v] = 0.f;
                 while (true) {
                     const bool valid = (rc + lane < re) && ((unsigned)(col - k0) < (unsigned)KC);
                     const unsigned bal = __ballot_sync(kFullMask, valid);
@@ -221,27 +239,49 @@ __global__ void __launch_bounds__(W * 32, 2)
                     const int q = npad / G;  // steps of each group
                     const int q4 = q & ~3;
                     const uint32_t gl = wl_addr + g * q * ENTRY;
+                    // The lane's words of the staged B row at byte offset off.
+                    auto load_b = [&](uint32_t off, uint32_t (&w)[NW]) {
+                        if constexpr (NCH == 0) {
+                            const uint2 b = lds64(stage + off);
+                            w[0] = b.x;
+                            w[1] = b.y;
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < NCH; ++c) {
+                                const uint4 b = lds128(stage + off + c * L * 16);
+                                w[4 * c] = b.x;
+                                w[4 * c + 1] = b.y;
+                                w[4 * c + 2] = b.z;
+                                w[4 * c + 3] = b.w;
+                            }
+                        }
+                    };
                     // One bf16 step: entry e = (stage offset / 8) | value << 16.
                     auto step_bf16 = [&](uint32_t e) {
-                        const uint2 b = lds64(stage + ((e & 0xffffu) << 3));
+                        uint32_t w[NW];
+                        load_b((e & 0xffffu) << 3, w);
                         const uint16_t av = hi16(e);
-                        acc[i][0] = fma_bf16(av, lo16(b.x), acc[i][0]);
-                        acc[i][1] = fma_bf16(av, hi16(b.x), acc[i][1]);
-                        acc[i][2] = fma_bf16(av, lo16(b.y), acc[i][2]);
-                        acc[i][3] = fma_bf16(av, hi16(b.y), acc[i][3]);
+#pragma unroll
+                        for (int q = 0; q < NW; ++q) {
+                            acc[i][2 * q] = fma_bf16(av, lo16(w[q]), acc[i][2 * q]);
+                            acc[i][2 * q + 1] = fma_bf16(av, hi16(w[q]), acc[i][2 * q + 1]);
+                        }
                     };
                     // One fp32 step: staged row at byte offset off, value bits av.
-                    auto step_f32 = [&](const uint4& b, uint32_t av) {
+                    auto step_f32 = [&](uint32_t off, uint32_t av) {
+                        uint32_t w[NW];
+                        load_b(off, w);
                         const float x = __uint_as_float(av);
                         const float2 a2 = make_float2(x, x);
-                        float2 lo = make_float2(c4[0], c4[1]), hi = make_float2(c4[2], c4[3]);
-                        lo = __ffma2_rn(a2, make_float2(__uint_as_float(b.x), __uint_as_float(b.y)), lo);
-                        hi = __ffma2_rn(a2, make_float2(__uint_as_float(b.z), __uint_as_float(b.w)), hi);
-                        c4[0] = lo.x;
-                        c4[1] = lo.y;
-                        c4[2] = hi.x;
-                        c4[3] = hi.y;
+#pragma unroll
+                        for (int q = 0; q < NW; q += 2) {
+                            float2 c2 = make_float2(c4[q], c4[q + 1]);
+                            c2 = __ffma2_rn(a2, make_float2(__uint_as_float(w[q]), __uint_as_float(w[q + 1])), c2);
+                            c4[q] = c2.x;
+                            c4[q + 1] = c2.y;
+                        }
                     };
+#pragma unroll 1
 #pragma unroll 1
                     for (int t = 0; t < q4; t += 4) {
                         if constexpr (BF) {
@@ -253,12 +293,10 @@ __global__ void __launch_bounds__(W * 32, 2)
                         } else {
                             const uint4 e01 = lds128(gl + t * 8);
                             const uint4 e23 = lds128(gl + t * 8 + 16);
-                            const uint4 b0 = lds128(stage + e01.x), b1 = lds128(stage + e01.z);
-                            const uint4 b2 = lds128(stage + e23.x), b3 = lds128(stage + e23.z);
-                            step_f32(b0, e01.y);
-                            step_f32(b1, e01.w);
-                            step_f32(b2, e23.y);
-                            step_f32(b3, e23.w);
+                            step_f32(e01.x, e01.y);
+                            step_f32(e01.z, e01.w);
+                            step_f32(e23.x, e23.y);
+                            step_f32(e23.z, e23.w);
                         }
                     }
 #pragma unroll 1
@@ -267,13 +305,13 @@ __global__ void __launch_bounds__(W * 32, 2)
                             step_bf16(lds32(gl + t * 4));
                         } else {
                             const uint2 e = lds64(gl + t * 8);
-                            step_f32(lds128(stage + e.x), e.y);
+                            step_f32(e.x, e.y);
                         }
                     }
                     __syncwarp();
                     if constexpr (!BF) {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
+                        for (int v = 0; v < VEC; ++v) {
                             cc[v] += c4[v];
                             c4[v] = 0.f;
                         }
@@ -284,7 +322,7 @@ __global__ void __launch_bounds__(W * 32, 2)
                 }
                 if constexpr (!BF) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) acc[i][v] += cc[v];
+                    for (int v = 0; v < VEC; ++v) acc[i][v] += cc[v];
                 }
                 if (lane == i) cur = rc;
                 if (i + 1 == R)
@@ -319,7 +357,7 @@ __global__ void __launch_bounds__(W * 32, 2)
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
+        for (int v = 0; v < VEC; ++v) {
             float x = acc[i][v];
             if (G >= 2) x += __shfl_xor_sync(kFullMask, x, L);
             if (G >= 4) x += __shfl_xor_sync(kFullMask, x, 2 * L);
@@ -331,14 +369,17 @@ __global__ void __launch_bounds__(W * 32, 2)
     for (int i = 0; i < R; ++i) {
         const int row = __shfl_sync(kFullMask, my_row, i);
         if (row < 0 || g != 0) continue;
-        const int c0 = n0 + l * 4;
-        float* dst = a.C + (long long)row * a.ldc + c0;
-        if (c0 + 4 <= a.N) {
-            *reinterpret_cast<float4*>(dst) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        } else {
+        float* crow = a.C + (long long)row * a.ldc + n0;
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                if (c0 + v < a.N) dst[v] = acc[i][v];
+        for (int v = 0; v < VEC; v += 4) {  // 4 contiguous columns at a time
+            const int c = lane_col<L, VEC, C_::ES>(l, v);
+            if (n0 + c + 4 <= a.N) {
+                *reinterpret_cast<float4*>(crow + c) = make_float4(acc[i][v], acc[i][v + 1], acc[i][v + 2], acc[i][v + 3]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (n0 + c + u < a.N) crow[c + u] = acc[i][v + u];
+            }
         }
     }
 }
@@ -352,12 +393,12 @@ __global__ void fill_f32_kernel(float* C, int M, int N, long long ldc) {
     }
 }
 
-template <bool BF, int L, int R, int W, int KC, int NS>
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS>
 int launch_cfg(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
-    using C_ = SpmmCfg<BF, L, R, W, KC, NS>;
+    using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::NT, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = spmm_kernel<BF, L, R, W, KC, NS>;
+    auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS>;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -386,23 +427,32 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
     return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
 }
 
-// Tile choice: 128 output columns per CTA (4 per lane), or 64 when N ≤ 64;
-// 4 rows per warp and 16 warps (64 rows per CTA), two CTAs per SM and one
-// 96 KB stage per CTA: while one CTA waits for its next chunk the other
-// computes, and the tall chunks (KC = 192 fp32 / 384 bf16 rows) halve the
-// per-(row, chunk) work that a double-buffered 2 x 48 KB layout needs
-// (measured: FFN step 7.69 against 8.90 ms).
+// Tile choice.  Lanes own 8 elements of a 256-column strip when N > 128
+// (fp32: two 16-byte loads per step, 2 rows per warp to fit 64 registers;
+// bf16: one 16-byte load, 4 rows per warp); 4 elements of a 128- or
+// 64-column strip for narrower N.  16 warps, two CTAs per SM, 96 KB of
+// stage per CTA.  One tall stage (the default) against two stages of half
+// the height: the FFN step took 7.69 against 8.90 ms (per-(row, chunk) work
+// halves).
 #ifndef USM_SPMM_STAGES
 #define USM_SPMM_STAGES 1
 #endif
 int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
-    constexpr int W = 16, R = 4, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
+    constexpr int W = 16, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
+    // 4 rows per warp unless that leaves fewer than ~3 CTAs per SM.
+    const int sms = sm_count_current_device();
+    auto few = [&](int nt, int mt) {
+        return (long long)((a.M + mt - 1) / mt) * ((a.N + nt - 1) / nt) < 3LL * sms;
+    };
     if (!bf16) {
-        if (a.N <= 64) return launch_cfg<false, 16, R, W, 192 * F, NS>(a, B, ldb, stream);
-        return launch_cfg<false, 32, R, W, 96 * F, NS>(a, B, ldb, stream);
+        if (a.N <= 64) return launch_cfg<false, 16, 4, 4, W, 192 * F, NS>(a, B, ldb, stream);
+        if (a.N <= 128) return launch_cfg<false, 32, 4, 4, W, 96 * F, NS>(a, B, ldb, stream);
+        return launch_cfg<false, 32, 8, 2, W, 48 * F, NS>(a, B, ldb, stream);
     }
-    if (a.N <= 64) return launch_cfg<true, 16, R, W, 384 * F, NS>(a, B, ldb, stream);
-    return launch_cfg<true, 32, R, W, 192 * F, NS>(a, B, ldb, stream);
+    if (a.N <= 64) return launch_cfg<true, 16, 4, 4, W, 384 * F, NS>(a, B, ldb, stream);
+    if (a.N <= 128) return launch_cfg<true, 32, 4, 4, W, 192 * F, NS>(a, B, ldb, stream);
+    if (few(256, 4 * W)) return launch_cfg<true, 32, 8, 2, W, 96 * F, NS>(a, B, ldb, stream);
+    return launch_cfg<true, 32, 8, 4, W, 96 * F, NS>(a, B, ldb, stream);
 }
 
 }  // namespace usm
