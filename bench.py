@@ -168,6 +168,27 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# Replicas over ranks (one GPU each; no data exchange)
+# ---------------------------------------------------------------------------
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest
+    replica's).  Uses the default process group; the tensor lives on
+    `device` (the rank's GPU under NCCL, CPU under gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job rate: the units all ranks processed over the slowest rank's
+    time (weak scaling: every replica runs the same step)."""
+    return units_per_rank_step * steps * world / (max_ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
 def run_ours(args, rank, world, local_rank):
@@ -289,14 +310,11 @@ def run_ours(args, rank, world, local_rank):
     per_launch_ms = {label: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
                      for i, (label, _, _) in enumerate(launches)}
 
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
     step_flops = sum(flops_of(d["p"], op) for _, op, d in launches)
     step_bytes = sum(alg_bytes(d["p"], op) for _, op, d in launches)
-    value = step_flops * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    value = job_throughput(step_flops, args.steps, world, elapsed_ms) / 1e9
 
     # Dominant launch (largest time) and its roofline.
     rows = []
