@@ -255,12 +255,13 @@ def run_ours(args, rank, world, local_rank):
     def run_one(op, d):
         K = d["p"].csr.K
         if wl == "attention":
+            seg = d["p"].meta["seq"]
             if op == "sddmm":
-                usm.sddmm(d["ro"], d["ci"], d["X"], d["Y"], row_swizzle=d["perm"], out=d["S"])
+                usm.sddmm(d["ro"], d["ci"], d["X"], d["Y"], row_swizzle=d["perm"], out=d["S"], seg_rows=seg)
             elif op == "softmax":
                 usm.row_softmax(d["ro"], d["S"], out=d["P"])
             else:
-                usm.spmm(d["ro"], d["ci"], d["P"], d["V"], K=K, row_swizzle=d["perm"], out=d["C"])
+                usm.spmm(d["ro"], d["ci"], d["P"], d["V"], K=K, row_swizzle=d["perm"], out=d["C"], seg_rows=seg)
         elif op == "spmm":
             usm.spmm(d["ro"], d["ci"], d["vals"], d["B"], K=K, row_swizzle=d["perm"], out=d["C"])
         elif op == "sddmm":

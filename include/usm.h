@@ -71,12 +71,17 @@ typedef enum usm_status {
  *       in which rows are scheduled (see row_swizzle_build).  It changes only
  *       the schedule, never the result (each output row is computed by one
  *       unit in a fixed order).
+ *   seg_rows : the rows per diagonal block the swizzle was built with (the
+ *       seg_rows of row_swizzle_build); <= 0 or > M means one block.  The row
+ *       scheduler deals each block's swizzled rows out to thread blocks so
+ *       that every thread block gets a similar mix of row lengths and never
+ *       rows of two blocks.  Like the swizzle, it never changes the result.
  * Limits: 0 ≤ M, K, N < 2^31, nnz < 2^31; ldc a multiple of 4.
  * Empty cases: M = 0 or N = 0 is a no-op; nnz = 0 zero-fills C.
  */
 int csr_spmm(int M, int K, int N, int nnz,
              const int *row_offsets, const int *col_indices, const void *values,
-             const int *row_swizzle,
+             const int *row_swizzle, int seg_rows,
              const void *B, int ldb,
              float *C, int ldc,
              usm_dtype dtype, void *stream);
@@ -96,7 +101,7 @@ int csr_spmm(int M, int K, int N, int nnz,
  *   out  : [nnz] in the mask's CSR order, element type `out_dtype`
  *          (USM_F32, or USM_BF16 rounded to nearest even from the fp32 sum):
  *          out[p] = Σ_{j<D} X[r][j] · Y[col_indices[p]][j],  p in row r.
- *   row_swizzle : NULL or a permutation of 0..M-1 (schedule only).
+ *   row_swizzle, seg_rows : as csr_spmm (schedule only).
  *   workspace : device scratch of at least
  *          csr_sddmm_workspace_bytes(M, K, D, nnz, in_dtype) bytes; may be
  *          NULL when that size is 0.  Its contents on entry are ignored.
@@ -106,7 +111,7 @@ size_t csr_sddmm_workspace_bytes(int M, int K, int D, int nnz, usm_dtype in_dtyp
 
 int csr_sddmm(int M, int K, int D, int nnz,
               const int *row_offsets, const int *col_indices,
-              const int *row_swizzle,
+              const int *row_swizzle, int seg_rows,
               const void *X, int ldx,
               const void *Y, int ldy,
               void *out, usm_dtype in_dtype, usm_dtype out_dtype,
@@ -141,7 +146,7 @@ int csr_sddmm(int M, int K, int D, int nnz,
  */
 int csr_sddmm_static_scratch(int M, int K, int D, int nnz,
                              const int *row_offsets, const int *col_indices,
-                             const int *row_swizzle,
+                             const int *row_swizzle, int seg_rows,
                              const void *X, int ldx,
                              const void *Y, int ldy,
                              void *out, usm_dtype in_dtype, usm_dtype out_dtype,
@@ -191,7 +196,7 @@ size_t csr_sddmm_general_workspace_bytes(int M, int K, int D, int nnz, usm_dtype
 
 int csr_sddmm_general(int M, int K, int D, int nnz,
                       const int *row_offsets, const int *col_indices, const void *values,
-                      const int *row_swizzle,
+                      const int *row_swizzle, int seg_rows,
                       const void *X, int ldx,
                       const void *Y, int ldy, int y_transposed,
                       void *out, usm_dtype in_dtype, usm_dtype out_dtype,

@@ -73,7 +73,7 @@ def test_workspace_sizes(lib):
 
 
 def spmm(lib, M=4, K=4, N=8, nnz=4, ro=A16, ci=A16, vals=A16, perm=None, B=A16, ldb=8, C=A16, ldc=8, dt=0):
-    return lib.csr_spmm(M, K, N, nnz, ro, ci, vals, perm, B, ldb, C, ldc, dt, None)
+    return lib.csr_spmm(M, K, N, nnz, ro, ci, vals, perm, 0, B, ldb, C, ldc, dt, None)
 
 
 def test_spmm_rejects_bad_args_on_host(lib):
@@ -99,7 +99,7 @@ def test_spmm_rejects_bad_args_on_host(lib):
 
 def sddmm(lib, M=4, K=4, D=8, nnz=4, ro=A16, ci=A16, perm=None, X=A16, ldx=8, Y=A16, ldy=8, out=A16,
           it=0, ot=0, ws=None, wsb=0):
-    return lib.csr_sddmm(M, K, D, nnz, ro, ci, perm, X, ldx, Y, ldy, out, it, ot, ws, wsb, None)
+    return lib.csr_sddmm(M, K, D, nnz, ro, ci, perm, 0, X, ldx, Y, ldy, out, it, ot, ws, wsb, None)
 
 
 def test_sddmm_rejects_bad_args_on_host(lib):
@@ -138,7 +138,7 @@ def test_next_rows_reject_bad_args_on_host(lib):
     assert lib.csr_permute_values(5, None, A16, 0, A16, None) == -1
     assert lib.csr_permute_values(0, None, None, 0, None, None) == 0
     g = lambda **k: lib.csr_sddmm_general(*[k.get(n, v) for n, v in [
-        ("M", 4), ("K", 4), ("D", 8), ("nnz", 4), ("ro", A16), ("ci", A16), ("vals", None), ("perm", None),
+        ("M", 4), ("K", 4), ("D", 8), ("nnz", 4), ("ro", A16), ("ci", A16), ("vals", None), ("perm", None), ("seg", 0),
         ("X", A16), ("ldx", 8), ("Y", A16), ("ldy", 8), ("ytr", 1), ("out", A16), ("it", 0), ("ot", 0),
         ("ws", None), ("wsb", 0), ("st", None)]])
     assert g(ytr=2) == -1

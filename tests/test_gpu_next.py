@@ -143,9 +143,10 @@ def test_attention_chain_with_softmax(usm):
     csr = p.csr
     ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
     perm = usm.row_swizzle(ro, csr.K, seg_rows=p.meta["seq"])
-    scores = usm.sddmm(ro, ci, dev(p.X, "bf16"), dev(p.Y, "bf16"), row_swizzle=perm)
+    seg = p.meta["seq"]
+    scores = usm.sddmm(ro, ci, dev(p.X, "bf16"), dev(p.Y, "bf16"), row_swizzle=perm, seg_rows=seg)
     probs = usm.row_softmax(ro, scores, out_dtype=torch.bfloat16)
-    O = host(usm.spmm(ro, ci, probs, dev(p.V, "bf16"), K=csr.K, row_swizzle=perm))
+    O = host(usm.spmm(ro, ci, probs, dev(p.V, "bf16"), K=csr.K, row_swizzle=perm, seg_rows=seg))
     rows = sample_rows(csr.M, 128, 120, host(perm))
     sub_ro, sub_ci, pos = oracle.select_rows(csr.row_offsets, csr.col_indices, rows)
     Xw = oracle.widen(p.X, "bf16")[rows]

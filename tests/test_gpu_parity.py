@@ -304,9 +304,10 @@ def test_attention_chain(usm):
     ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
     perm = usm.row_swizzle(ro, csr.K, seg_rows=p.meta["seq"])
     Q, Kt, V = dev(p.X, "bf16"), dev(p.Y, "bf16"), dev(p.V, "bf16")
-    s32 = usm.sddmm(ro, ci, Q, Kt, row_swizzle=perm)
-    s16 = usm.sddmm(ro, ci, Q, Kt, row_swizzle=perm, out_dtype=torch.bfloat16)
-    O = host(usm.spmm(ro, ci, s16, V, K=csr.K, row_swizzle=perm))
+    seg = p.meta["seq"]
+    s32 = usm.sddmm(ro, ci, Q, Kt, row_swizzle=perm, seg_rows=seg)
+    s16 = usm.sddmm(ro, ci, Q, Kt, row_swizzle=perm, out_dtype=torch.bfloat16, seg_rows=seg)
+    O = host(usm.spmm(ro, ci, s16, V, K=csr.K, row_swizzle=perm, seg_rows=seg))
     rows = sample_rows(csr.M, 128, 110, host(perm))
     # scores
     ref_s, S_s, pos = oracle_sddmm(csr, p.X, p.Y, "bf16", rows)
@@ -348,9 +349,39 @@ def test_misaligned_pointer_rejected(usm):
     B = torch.zeros((10, 9), device="cuda")[:, 1:]   # offset by 4 bytes, ld 9
     C = torch.zeros((10, 8), device="cuda")
     lib = usm.load()
-    code = lib.csr_spmm(10, 10, 8, csr.nnz, ro.data_ptr(), ci.data_ptr(), vals.data_ptr(), None,
+    code = lib.csr_spmm(10, 10, 8, csr.nnz, ro.data_ptr(), ci.data_ptr(), vals.data_ptr(), None, 0,
                         B.data_ptr(), 9, C.data_ptr(), 8, 0, usm._stream())
     assert code == -2
     # the binding pads such operands itself and gets the right answer
     Cb = host(usm.spmm(ro, ci, vals, B, K=10))
     assert np.array_equal(Cb, np.zeros((10, 8), np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_scheduler_does_not_change_bits(usm, dtype):
+    """Block-diagonal matrix with skewed (lognormal) rows: the results are
+    bit-identical with no swizzle, a global swizzle, and per-block swizzle
+    and schedule (each output is computed by one unit in a fixed order)."""
+    blocks, seq, D = 5, 700, 96
+    rng = np.random.default_rng(130)
+    lens = W.lengths_lognormal(rng, blocks * seq, seq, 60.0, 0.8)
+    base = (np.arange(blocks * seq) // seq) * seq
+    ro, ci = W.csr_from_lengths(rng, lens, seq, col_base=base)
+    vals = W.values_for(rng, int(ro[-1]), 1.0, dtype)
+    csr = W.CSR(blocks * seq, blocks * seq, ro, ci, vals, dtype, seg_rows=seq)
+    B = W.dense(rng, csr.K, D, 1.0, dtype)
+    X = W.dense(rng, csr.M, D, 1.0, dtype)
+    rod, cid, vd = csr_dev(csr)
+    Bd, Xd = dev(B, dtype), dev(X, dtype)
+    variants = [(None, 0), (usm.row_swizzle(rod, csr.K), 0), (usm.row_swizzle(rod, csr.K, seq), seq),
+                (usm.row_swizzle(rod, csr.K, seq), 0)]
+    Cs = [host(usm.spmm(rod, cid, vd, Bd, K=csr.K, row_swizzle=p, seg_rows=s)) for p, s in variants]
+    Ss = [host(usm.sddmm(rod, cid, Xd, Bd, row_swizzle=p, seg_rows=s)) for p, s in variants]
+    for c in Cs[1:]:
+        assert np.array_equal(c, Cs[0])
+    for o in Ss[1:]:
+        assert np.array_equal(o, Ss[0])
+    ref, S = oracle_spmm(csr, B, dtype)
+    assert_within(Cs[0], ref, S, TOL[dtype], "block-diagonal spmm")
+    ref, S, _ = oracle_sddmm(csr, X, B, dtype)
+    assert_within(Ss[0], ref, S, TOL[dtype], "block-diagonal sddmm")

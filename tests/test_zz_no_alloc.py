@@ -20,7 +20,7 @@ STATIC_SCRATCH_BYTES = 32 << 20
 def _call_static(lib, usm, ro, ci, csr, Xd, Yd, out, in_code, out_code):
     D = Xd.shape[1]
     return lib.csr_sddmm_static_scratch(
-        csr.M, csr.K, D, csr.nnz, ro.data_ptr(), ci.data_ptr(), None,
+        csr.M, csr.K, D, csr.nnz, ro.data_ptr(), ci.data_ptr(), None, 0,
         Xd.data_ptr(), Xd.stride(0), Yd.data_ptr(), Yd.stride(0), out.data_ptr(), in_code, out_code,
         usm._stream())
 
@@ -57,6 +57,6 @@ def test_static_scratch_rejects_oversized_problem(usm):
     assert lib.csr_sddmm_workspace_bytes(M, K, D, nnz, 0) > STATIC_SCRATCH_BYTES
     # Rejected on the host before any launch; the pointers are never read.
     fake = 0x10000
-    code = lib.csr_sddmm_static_scratch(M, K, D, nnz, fake, fake, None, fake, D, fake, D, fake, 0, 0,
+    code = lib.csr_sddmm_static_scratch(M, K, D, nnz, fake, fake, None, 0, fake, D, fake, D, fake, 0, 0,
                                         usm._stream())
     assert code == -3

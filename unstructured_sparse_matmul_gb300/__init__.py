@@ -28,19 +28,19 @@ STATUS = {
 # Every symbol include/usm.h declares, with its ctypes signature.
 _vp, _i, _sz, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_longlong
 SIGNATURES = {
-    "csr_spmm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _vp]),
+    "csr_spmm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _vp]),
     "csr_sddmm_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
-    "csr_sddmm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _vp, _sz, _vp]),
+    "csr_sddmm": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _vp, _i, _i, _vp, _sz, _vp]),
     "row_swizzle_workspace_bytes": (_sz, [_i, _i]),
     "row_swizzle_build": (_i, [_i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "usm_poll_status": (_i, [_vp]),
     "usm_status_string": (ctypes.c_char_p, [_i]),
     "usm_selftest_wait_timeout": (_i, [_ll, _vp]),
-    "csr_sddmm_static_scratch": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _vp]),
+    "csr_sddmm_static_scratch": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _vp, _i, _i, _vp]),
     "csr_transpose_workspace_bytes": (_sz, [_i, _i, _i]),
     "csr_sddmm_general_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
-    "csr_sddmm_general": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _vp, _i, _i, _vp, _sz,
-                               _vp]),
+    "csr_sddmm_general": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _vp, _i, _i, _vp,
+                               _sz, _vp]),
     "csr_row_softmax": (_i, [_i, _i, _vp, _vp, _vp, _i, _vp]),
     "csr_transpose": (_i, [_i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "csr_permute_values": (_i, [_i, _vp, _vp, _i, _vp, _vp]),
@@ -174,7 +174,7 @@ def row_swizzle(row_offsets, K: int, seg_rows: int = 0, out=None, stream=None):
 
 
 def spmm(row_offsets, col_indices, values, B, K: int | None = None, row_swizzle=None, out=None,
-         stream=None):
+         stream=None, seg_rows: int = 0):
     """C = A·B (fp32 out).  values and B are both fp32 or both bf16."""
     torch = _torch()
     lib = load()
@@ -189,14 +189,14 @@ def spmm(row_offsets, col_indices, values, B, K: int | None = None, row_swizzle=
     C = out if out is not None else _new_dense_out(M, N, B.device)
     _require(C, "out", (torch.float32,))
     code = lib.csr_spmm(M, K, N, col_indices.numel(), _ptr(row_offsets), _ptr(col_indices), _ptr(values),
-                        _ptr(row_swizzle), _ptr(B), _ld(B), _ptr(C), _ld(C), _dtype_code(values),
+                        _ptr(row_swizzle), seg_rows, _ptr(B), _ld(B), _ptr(C), _ld(C), _dtype_code(values),
                         _stream(stream))
     _check("csr_spmm", code)
     return C
 
 
 def sddmm(row_offsets, col_indices, X, Y, row_swizzle=None, out=None, out_dtype=None, workspace=None,
-          stream=None):
+          stream=None, seg_rows: int = 0):
     """out[p] = X[r]·Y[col_p] on the mask's nonzeros (CSR order)."""
     torch = _torch()
     lib = load()
@@ -218,7 +218,7 @@ def sddmm(row_offsets, col_indices, X, Y, row_swizzle=None, out=None, out_dtype=
     ws_bytes = lib.csr_sddmm_workspace_bytes(M, K, D, nnz, in_code)
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=X.device)
-    code = lib.csr_sddmm(M, K, D, nnz, _ptr(row_offsets), _ptr(col_indices), _ptr(row_swizzle),
+    code = lib.csr_sddmm(M, K, D, nnz, _ptr(row_offsets), _ptr(col_indices), _ptr(row_swizzle), seg_rows,
                          _ptr(X), _ld(X), _ptr(Y), _ld(Y), _ptr(out), in_code, out_code,
                          _ptr(workspace) if ws_bytes else None, ws_bytes, _stream(stream))
     _check("csr_sddmm", code)
@@ -226,7 +226,7 @@ def sddmm(row_offsets, col_indices, X, Y, row_swizzle=None, out=None, out_dtype=
 
 
 def sddmm_general(row_offsets, col_indices, X, Y, values=None, y_transposed=True, row_swizzle=None, out=None,
-                  out_dtype=None, stream=None):
+                  out_dtype=None, stream=None, seg_rows: int = 0):
     """out[p] = (values[p] if given) · X[r]·Yop[col_p]; Yop = Y (K×D) when
     y_transposed, else Yᵀ with Y given D×K."""
     torch = _torch()
@@ -254,7 +254,8 @@ def sddmm_general(row_offsets, col_indices, X, Y, values=None, y_transposed=True
     ws_bytes = lib.csr_sddmm_general_workspace_bytes(M, K, D, nnz, in_code, int(bool(y_transposed)))
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=X.device)
     code = lib.csr_sddmm_general(M, K, D, nnz, _ptr(row_offsets), _ptr(col_indices), _ptr(values),
-                                 _ptr(row_swizzle), _ptr(X), _ld(X), _ptr(Y), Y.stride(0), int(bool(y_transposed)),
+                                 _ptr(row_swizzle), seg_rows, _ptr(X), _ld(X), _ptr(Y), Y.stride(0),
+                                 int(bool(y_transposed)),
                                  _ptr(out), in_code, _dtype_code(out), _ptr(ws) if ws_bytes else None, ws_bytes,
                                  _stream(stream))
     _check("csr_sddmm_general", code)

@@ -97,8 +97,8 @@ using namespace usm;
 extern "C" {
 
 int csr_spmm(int M, int K, int N, int nnz, const int* row_offsets, const int* col_indices,
-             const void* values, const int* row_swizzle, const void* B, int ldb, float* C, int ldc,
-             usm_dtype dtype, void* stream) {
+             const void* values, const int* row_swizzle, int seg_rows, const void* B, int ldb, float* C,
+             int ldc, usm_dtype dtype, void* stream) {
     if (M < 0 || K < 0 || N < 0 || nnz < 0) return USM_ERR_INVALID_ARG;
     if (dtype != USM_F32 && dtype != USM_BF16) return USM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return USM_OK;
@@ -114,7 +114,8 @@ int csr_spmm(int M, int K, int N, int nnz, const int* row_offsets, const int* co
     if (!aligned16(B) || ((long long)ldb * es) % 16 != 0) return USM_ERR_ALIGNMENT;
     int* status = status_word_for_current_device();
     if (!status) return USM_ERR_CUDA;
-    SpmmArgs a{M, K, N, nnz, row_offsets, col_indices, values, row_swizzle, C, ldc, status};
+    SpmmArgs a{M, K, N, nnz, row_offsets, col_indices, values, row_swizzle, effective_seg(M, seg_rows), C, ldc,
+               status};
     return launch_spmm(a, B, ldb, dtype == USM_BF16, st);
 }
 
@@ -124,7 +125,7 @@ size_t csr_sddmm_workspace_bytes(int M, int K, int D, int nnz, usm_dtype in_dtyp
 }
 
 int csr_sddmm(int M, int K, int D, int nnz, const int* row_offsets, const int* col_indices,
-              const int* row_swizzle, const void* X, int ldx, const void* Y, int ldy, void* out,
+              const int* row_swizzle, int seg_rows, const void* X, int ldx, const void* Y, int ldy, void* out,
               usm_dtype in_dtype, usm_dtype out_dtype, void* workspace, size_t workspace_bytes,
               void* stream) {
     if (M < 0 || K < 0 || D < 0 || nnz < 0) return USM_ERR_INVALID_ARG;
@@ -145,7 +146,7 @@ int csr_sddmm(int M, int K, int D, int nnz, const int* row_offsets, const int* c
     if (need > 0 && !aligned16(workspace)) return USM_ERR_ALIGNMENT;
     int* status = status_word_for_current_device();
     if (!status) return USM_ERR_CUDA;
-    SddmmArgs a{M, K, D, nnz, row_offsets, col_indices, row_swizzle, X, ldx, out, 0,
+    SddmmArgs a{M, K, D, nnz, row_offsets, col_indices, row_swizzle, effective_seg(M, seg_rows), X, ldx, out, 0,
                 out_dtype == USM_BF16 ? 1 : 0, 1, status};
     return launch_sddmm(a, Y, ldy, in_dtype == USM_BF16, workspace, workspace_bytes, st);
 }
@@ -186,7 +187,8 @@ size_t csr_sddmm_general_workspace_bytes(int M, int K, int D, int nnz, usm_dtype
 }
 
 int csr_sddmm_general(int M, int K, int D, int nnz, const int* row_offsets, const int* col_indices,
-                      const void* values, const int* row_swizzle, const void* X, int ldx, const void* Y, int ldy,
+                      const void* values, const int* row_swizzle, int seg_rows, const void* X, int ldx,
+                      const void* Y, int ldy,
                       int y_transposed, void* out, usm_dtype in_dtype, usm_dtype out_dtype, void* workspace,
                       size_t workspace_bytes, void* stream) {
     if (M < 0 || K < 0 || D < 0 || nnz < 0) return USM_ERR_INVALID_ARG;
@@ -220,7 +222,7 @@ int csr_sddmm_general(int M, int K, int D, int nnz, const int* row_offsets, cons
         Yk = workspace;
     }
     if (ldyk > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
-    SddmmArgs a{M, K, D, nnz, row_offsets, col_indices, row_swizzle, X, ldx, out, 0,
+    SddmmArgs a{M, K, D, nnz, row_offsets, col_indices, row_swizzle, effective_seg(M, seg_rows), X, ldx, out, 0,
                 out_dtype == USM_BF16 ? 1 : 0, 1, status, values, bf ? 1 : 0};
     void* part = part_bytes ? static_cast<unsigned char*>(workspace) + yt_bytes : nullptr;
     return launch_sddmm(a, Yk, (int)ldyk, bf, part, part_bytes, st);

@@ -140,6 +140,25 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
+// Row scheduler.  The row swizzle lists rows by decreasing length (inside
+// each diagonal block of seg rows); the kernels map swizzled positions to
+// (row tile, slot) in a boustrophedon order: tile t of a block takes
+// positions t, 2T-1-t, 2T+t, ... (T tiles per block), so every tile gets a
+// similar mix of long and short rows, and a tile never spans two blocks.
+// Slots alternate over the warps the same way.  Returns the position in the
+// swizzle, or -1 past the block or the matrix.
+__device__ __forceinline__ long long sched_pos(int tile, int slot, int MT, int seg, int M) {
+    const int T = (seg + MT - 1) / MT;  // tiles per block
+    const int b = tile / T, t = tile - b * T;
+    const long long p = (long long)slot * T + ((slot & 1) ? (T - 1 - t) : t);
+    if (p >= seg) return -1;
+    const long long m = (long long)b * seg + p;
+    return m < M ? m : -1;
+}
+__device__ __forceinline__ int sched_slot(int i, int warp, int W) {
+    return i * W + ((i & 1) ? (W - 1 - warp) : warp);
+}
+
 // Read-only streaming loads of CSR arrays.
 __device__ __forceinline__ int ldg_i32(const int* p) { return __ldg(p); }
 

@@ -16,6 +16,7 @@ struct SpmmArgs {
     const int* col_indices;
     const void* values;
     const int* perm;  // may be null (identity order)
+    int seg_rows;     // rows per diagonal block of the schedule (> 0)
     float* C;
     long long ldc;
     int* status;
@@ -26,6 +27,7 @@ struct SddmmArgs {
     const int* row_offsets;
     const int* col_indices;
     const int* perm;
+    int seg_rows;
     const void* X;
     long long ldx;
     void* out;           // final output (single strip) or fp32 partials (several strips)
@@ -89,6 +91,12 @@ int launch_csr_transpose(int M, int K, int nnz, const int* row_offsets, const in
                          void* ws, size_t ws_bytes, cudaStream_t stream);
 int launch_permute_values(int nnz, const int* perm, const void* values, bool bf16, void* out,
                           cudaStream_t stream);
+
+// Row tiles of MT rows when tiles may not span blocks of seg rows.
+inline long long schedule_tiles(int M, int seg, int MT) {
+    return (long long)((M + seg - 1) / seg) * ((seg + MT - 1) / MT);
+}
+inline int effective_seg(int M, int seg_rows) { return (seg_rows <= 0 || seg_rows > M) ? M : seg_rows; }
 
 int launch_wait_timeout_selftest(long long limit_ns, int* status, cudaStream_t stream);
 

@@ -6,8 +6,9 @@
 // the product is X·Yᵀ), the form weight gradients and sparse-attention
 // scores need.  GB300 design:
 //
-// * Tiles.  A CTA owns MT = R·W mask rows (row-swizzle order, R chosen at
-//   launch) and one strip of DT columns of D.  It walks K in chunks of KC
+// * Tiles.  A CTA owns MT = R·W mask rows (dealt from the row-swizzle order
+//   by the row scheduler, sched_pos; R chosen at launch) and one strip of DT
+//   columns of D.  It walks K in chunks of KC
 //   rows; one thread copies Y[k0:k0+KC, d0:d0+DT] into a shared-memory stage
 //   with TMA (mbarrier, bounded wait).  One 96 KB stage per CTA and two CTAs
 //   per SM: the tall chunks halve the per-(row, chunk) work of a
@@ -166,8 +167,8 @@ __global__ void __launch_bounds__(W * 32, MINB)
 
     int my_row = -1, my_start = 0, my_end = 0;
     if (lane < R) {
-        const long long m = (long long)tile * MT + (long long)lane * W + warp;
-        if (m < a.M) {
+        const long long m = sched_pos(tile, sched_slot(lane, warp, W), MT, a.seg_rows, a.M);
+        if (m >= 0) {
             const int r = a.perm ? __ldg(a.perm + m) : (int)m;
             if ((unsigned)r < (unsigned)a.M) {
                 int s = __ldg(a.row_offsets + r), e = __ldg(a.row_offsets + r + 1);
@@ -387,9 +388,11 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     // (two resident at a time), up to 32.
     const int sms = sm_count_current_device();
     int R = 32;
-    while (R > 1 && (long long)((a.M + R * W - 1) / (R * W)) * nstrips < 4LL * MINB * sms / 2) R >>= 1;
+    while (R > 1 && schedule_tiles(a.M, a.seg_rows, R * W) * nstrips < 4LL * MINB * sms / 2) R >>= 1;
     a.rows_per_warp = R;
-    const dim3 grid((a.M + R * W - 1) / (R * W), nstrips);
+    const long long tiles = schedule_tiles(a.M, a.seg_rows, R * W);
+    if (tiles > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)tiles, nstrips);
     kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);
     if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
     if (nstrips > 1) {

@@ -47,9 +47,9 @@ int scratch_for_current_device(void** out) {
 }  // namespace
 
 extern "C" int csr_sddmm_static_scratch(int M, int K, int D, int nnz, const int* row_offsets,
-                                        const int* col_indices, const int* row_swizzle, const void* X,
-                                        int ldx, const void* Y, int ldy, void* out, usm_dtype in_dtype,
-                                        usm_dtype out_dtype, void* stream) {
+                                        const int* col_indices, const int* row_swizzle, int seg_rows,
+                                        const void* X, int ldx, const void* Y, int ldy, void* out,
+                                        usm_dtype in_dtype, usm_dtype out_dtype, void* stream) {
     const size_t need = csr_sddmm_workspace_bytes(M, K, D, nnz, in_dtype);
     if (need > kStaticScratchBytes) return USM_ERR_UNSUPPORTED;
     void* scratch = nullptr;
@@ -60,6 +60,6 @@ extern "C" int csr_sddmm_static_scratch(int M, int K, int D, int nnz, const int*
     // Every strip writes its partial for every nonzero before the strip sum
     // reads it, so nothing left in the array by an earlier call is ever read:
     // no clearing is needed.
-    return csr_sddmm(M, K, D, nnz, row_offsets, col_indices, row_swizzle, X, ldx, Y, ldy, out, in_dtype,
+    return csr_sddmm(M, K, D, nnz, row_offsets, col_indices, row_swizzle, seg_rows, X, ldx, Y, ldy, out, in_dtype,
                      out_dtype, scratch, need > 0 ? kStaticScratchBytes : 0, stream);
 }

@@ -6,9 +6,10 @@
 // work is split ("Interesting ideas" I4).  The design below is written for
 // GB300, not taken from the V100 kernels:
 //
-// * 1-D tiles.  A CTA owns MT = R·W rows of A (taken in row-swizzle order,
-//   interleaved across its W warps so every warp gets a similar share) and
-//   one strip of NT output columns.  Each output element is accumulated by
+// * 1-D tiles.  A CTA owns MT = R·W rows of A and one strip of NT output
+//   columns; the row scheduler (sched_pos) deals the row-swizzle order out to
+//   tiles and warps boustrophedon-fashion, so every tile and warp gets a
+//   similar mix of row lengths even when lengths are skewed.  Each output element is accumulated by
 //   exactly one lane group in a fixed order: results do not depend on the
 //   swizzle.  Two CTAs share an SM, so one CTA's barrier waits and prologue
 //   overlap the other's arithmetic.
@@ -129,8 +130,8 @@ __global__ void __launch_bounds__(W * 32, 2)
     // Row slots of this warp: slot i is row perm[tile*MT + i*W + warp].
     int my_row = -1, my_start = 0, my_end = 0;
     if (lane < R) {
-        const long long m = (long long)tile * C_::MT + (long long)lane * W + warp;
-        if (m < a.M) {
+        const long long m = sched_pos(tile, sched_slot(lane, warp, W), C_::MT, a.seg_rows, a.M);
+        if (m >= 0) {
             const int r = a.perm ? __ldg(a.perm + m) : (int)m;
             if ((unsigned)r < (unsigned)a.M) {
                 int s = __ldg(a.row_offsets + r), e = __ldg(a.row_offsets + r + 1);
@@ -410,7 +411,9 @@ int launch_cfg(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
     }
     // Row tiles on x (dispatched first, longest rows first under a swizzle),
     // column strips on y.
-    const dim3 grid((a.M + C_::MT - 1) / C_::MT, (a.N + C_::NT - 1) / C_::NT);
+    const long long tiles = schedule_tiles(a.M, a.seg_rows, C_::MT);
+    if (tiles > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
+    const dim3 grid((unsigned)tiles, (a.N + C_::NT - 1) / C_::NT);
     if (grid.y > 65535u) return USM_ERR_UNSUPPORTED;
     kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);
     return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
@@ -442,7 +445,7 @@ int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream
     // 4 rows per warp unless that leaves fewer than ~3 CTAs per SM.
     const int sms = sm_count_current_device();
     auto few = [&](int nt, int mt) {
-        return (long long)((a.M + mt - 1) / mt) * ((a.N + nt - 1) / nt) < 3LL * sms;
+        return schedule_tiles(a.M, a.seg_rows, mt) * ((a.N + nt - 1) / nt) < 3LL * sms;
     };
     if (!bf16) {
         if (a.N <= 64) return launch_cfg<false, 16, 4, 4, W, 192 * F, NS>(a, B, ldb, stream);
