@@ -264,6 +264,9 @@ __global__ void __launch_bounds__(W * 32, MINB)
                     const unsigned bal = __ballot_sync(kFullMask, valid);
                     const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);
                     if (n == 0) break;
+                    // A full window may continue: fetch the next one now so its
+                    // latency overlaps this window's work.
+                    const int ncol = (n == 32) ? window_col(a, rc + 32, re, lane) : INT_MAX;
                     wl[my_slot] = (lane < n) ? (uint32_t)(col - k0) * PITCH : 0u;
                     __syncwarp();
                     float part[L];
@@ -308,7 +311,7 @@ __global__ void __launch_bounds__(W * 32, MINB)
                     __syncwarp();
                     rc += n;
                     if (n < 32) break;
-                    col = window_col(a, rc, re, lane);
+                    col = ncol;
                 }
                 if (lane == i) cur = rc;
                 if (R == 1) {

@@ -223,6 +223,11 @@ __global__ void __launch_bounds__(W * 32, 2)
                     const unsigned bal = __ballot_sync(kFullMask, valid);
                     const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);  // valid prefix
                     if (n == 0) break;
+                    // A full window may continue: fetch the next one now so its
+                    // latency overlaps this window's work.
+                    int ncol = INT_MAX;
+                    uint32_t nval = 0;
+                    if (n == 32) load_window<BF>(a, rc + 32, re, lane, ncol, nval);
                     // G == 1: exact count (0-3 single steps at the end).  G > 1: each
                     // group's block must start 16-byte aligned for the 128-bit
                     // entry loads, so pad to a multiple of 4·G.
@@ -319,7 +324,8 @@ __global__ void __launch_bounds__(W * 32, 2)
                     }
                     rc += n;
                     if (n < 32) break;
-                    load_window<BF>(a, rc, re, lane, col, val);
+                    col = ncol;
+                    val = nval;
                 }
                 if constexpr (!BF) {
 #pragma unroll
