@@ -10,9 +10,11 @@
 //   by the row scheduler, sched_pos; R chosen at launch) and one strip of DT
 //   columns of D.  It walks K in chunks of KC
 //   rows; one thread copies Y[k0:k0+KC, d0:d0+DT] into a shared-memory stage
-//   with TMA (mbarrier, bounded wait).  One 96 KB stage per CTA and two CTAs
-//   per SM: the tall chunks halve the per-(row, chunk) work of a
-//   double-buffered layout, and the two CTAs cover each other's loads.
+//   with TMA (mbarrier, bounded wait) into one tall stage: the tall chunks
+//   halve the per-(row, chunk) work of a double-buffered layout.  bf16 runs
+//   two CTAs per SM with 96 KB each (latency-bound: the two CTAs cover each
+//   other's loads); fp32, bound by shared-memory bandwidth, runs one CTA per
+//   SM with a 192 KB stage and up to 128 registers.
 // * Per (row, chunk) a warp keeps X[r, d0:d0+DT] in registers (fp32), reads
 //   the row's next 32 column indices (coalesced window after its cursor),
 //   keeps the prefix inside the chunk and lists their stage offsets.
@@ -471,7 +473,8 @@ int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream) {
 int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, size_t ws_bytes,
                  cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SDDMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
-    if (!in_bf16) return launch_cfg<false, 8, 4, W, 96 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
+    // fp32: one CTA per SM, up to 128 registers, one 192 KB stage (KC = 384).
+    if (!in_bf16) return launch_cfg<false, 8, 4, W, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
     if (a.D <= 64) return launch_cfg<true, 8, 1, W, 384 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
     return launch_cfg<true, 8, 2, W, 192 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
 }

@@ -11,8 +11,9 @@
 //   tiles and warps boustrophedon-fashion, so every tile and warp gets a
 //   similar mix of row lengths even when lengths are skewed.  Each output element is accumulated by
 //   exactly one lane group in a fixed order: results do not depend on the
-//   swizzle.  Two CTAs share an SM, so one CTA's barrier waits and prologue
-//   overlap the other's arithmetic.
+//   swizzle.  bf16 runs two CTAs per SM, so one CTA's barrier waits and
+//   prologue overlap the other's arithmetic; fp32, bound by shared-memory
+//   bandwidth, runs one CTA per SM with more registers and a taller stage.
 // * Dense operand staging.  The CTA walks K in chunks of KC rows.  For each
 //   chunk one thread issues TMA tensor copies of B[k0:k0+KC, n0:n0+NT] into a
 //   shared-memory stage (completion on an mbarrier, bounded wait; one or two
@@ -99,8 +100,8 @@ __device__ __forceinline__ void load_window(const SpmmArgs& a, int pos, int end,
     }
 }
 
-template <bool BF, int L, int VEC, int R, int W, int KC, int NS>
-__global__ void __launch_bounds__(W * 32, 2)
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB>
+__global__ void __launch_bounds__(W * 32, MB)
     spmm_kernel(const __grid_constant__ CUtensorMap tmB, const SpmmArgs a) {
     using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
     constexpr int NCH = C_::NCH, NW = C_::NW;
@@ -400,12 +401,12 @@ __global__ void fill_f32_kernel(float* C, int M, int N, long long ldc) {
     }
 }
 
-template <bool BF, int L, int VEC, int R, int W, int KC, int NS>
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB>
 int launch_cfg(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
     using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::NT, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS>;
+    auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS, MB>;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -437,31 +438,42 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 }
 
 // Tile choice.  Lanes own 8 elements of a 256-column strip when N > 128
-// (fp32: two 16-byte loads per step, 2 rows per warp to fit 64 registers;
-// bf16: one 16-byte load, 4 rows per warp); 4 elements of a 128- or
-// 64-column strip for narrower N.  16 warps, two CTAs per SM, 96 KB of
-// stage per CTA.  One tall stage (the default) against two stages of half
-// the height: the FFN step took 7.69 against 8.90 ms (per-(row, chunk) work
-// halves).
+// (fp32: two 16-byte loads per step; bf16: one); 4 elements of a 128- or
+// 64-column strip for narrower N.  16 warps per CTA.  bf16 steps are
+// latency-bound and run two CTAs per SM (≤ 64 registers, 96 KB of stage
+// each); fp32 steps are bound by shared-memory bandwidth and run one CTA per
+// SM with up to 128 registers and one 192 KB stage (N > 128: KC = 192 rows
+// of 1 KB; N ≤ 128: 384 rows of 512 B): taller chunks halve the per-(row,
+// chunk) work and more rows per CTA share each staged row.  Measured against
+// two CTAs per SM: FFN fp32 SpMM 3-12% faster, LSTM (N = 128) 5% faster at
+// 50% sparsity up to 39% at 98%.  One tall stage (the default) against two
+// stages of half the height: the FFN step took 7.69 against 8.90 ms.
 #ifndef USM_SPMM_STAGES
 #define USM_SPMM_STAGES 1
 #endif
 int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
-    // 4 rows per warp unless that leaves fewer than ~3 CTAs per SM.
     const int sms = sm_count_current_device();
-    auto few = [&](int nt, int mt) {
-        return schedule_tiles(a.M, a.seg_rows, mt) * ((a.N + nt - 1) / nt) < 3LL * sms;
+    // One-CTA-per-SM launch time model for mt-row tiles of 256 columns: whole
+    // waves × per-CTA work, where a CTA stages every K row (weighted 2: a
+    // staged row costs about two consumed ones) and consumes mt mean rows.
+    auto cost = [&](int mt) {
+        const long long n = schedule_tiles(a.M, a.seg_rows, mt) * ((a.N + 255) / 256);
+        const double waves = (double)((n + sms - 1) / sms);
+        return waves * (2.0 * a.K + (double)mt * a.nnz / (a.M > 0 ? a.M : 1));
     };
     if (!bf16) {
-        if (a.N <= 64) return launch_cfg<false, 16, 4, 4, W, 192 * F, NS>(a, B, ldb, stream);
-        if (a.N <= 128) return launch_cfg<false, 32, 4, 4, W, 96 * F, NS>(a, B, ldb, stream);
-        return launch_cfg<false, 32, 8, 2, W, 48 * F, NS>(a, B, ldb, stream);
+        if (a.N <= 64) return launch_cfg<false, 16, 4, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
+        if (a.N <= 128) return launch_cfg<false, 32, 4, 4, W, 192 * F, NS, 1>(a, B, ldb, stream);
+        if (cost(2 * W) < cost(4 * W)) return launch_cfg<false, 32, 8, 2, W, 96 * F, NS, 1>(a, B, ldb, stream);
+        return launch_cfg<false, 32, 8, 4, W, 96 * F, NS, 1>(a, B, ldb, stream);
     }
-    if (a.N <= 64) return launch_cfg<true, 16, 4, 4, W, 384 * F, NS>(a, B, ldb, stream);
-    if (a.N <= 128) return launch_cfg<true, 32, 4, 4, W, 192 * F, NS>(a, B, ldb, stream);
-    if (few(256, 4 * W)) return launch_cfg<true, 32, 8, 2, W, 96 * F, NS>(a, B, ldb, stream);
-    return launch_cfg<true, 32, 8, 4, W, 96 * F, NS>(a, B, ldb, stream);
+    if (a.N <= 64) return launch_cfg<true, 16, 4, 4, W, 384 * F, NS, 2>(a, B, ldb, stream);
+    if (a.N <= 128) return launch_cfg<true, 32, 4, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
+    // 4 rows per warp unless that leaves fewer than ~3 CTAs per SM.
+    if (schedule_tiles(a.M, a.seg_rows, 4 * W) * ((a.N + 255) / 256) < 3LL * sms)
+        return launch_cfg<true, 32, 8, 2, W, 96 * F, NS, 2>(a, B, ldb, stream);
+    return launch_cfg<true, 32, 8, 4, W, 96 * F, NS, 2>(a, B, ldb, stream);
 }
 
 }  // namespace usm
