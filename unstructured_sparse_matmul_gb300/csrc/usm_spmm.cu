@@ -61,15 +61,21 @@ struct SpmmCfg {
     static constexpr int MT = R * W;
     static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
     static constexpr int THREADS = W * 32;
-    static constexpr int ENTRY = BF ? 4 : 8;       // list entry bytes
+    // List entries.  fp32: (stage offset, value bits), 8 bytes.  bf16 with
+    // 8-byte lane slices (ADDR): an array of shared-memory row addresses and
+    // one of bf16 values, 6 bytes, so a step needs one add for its address.
+    // bf16 with 16-byte slices: offset/8 | value << 16 in 4 bytes (the extra
+    // value load of the split form cost more than its saved arithmetic there).
+    static constexpr bool ADDR = BF && NCH == 0;
+    static constexpr int ENTRY = ADDR ? 6 : (BF ? 4 : 8);
     static constexpr int LIST_BYTES = W * 32 * ENTRY;
     static constexpr int SMEM = NS * STAGE + 64 + LIST_BYTES;
     static_assert(NS == 1 || NS == 2, "one or two stages");
     static_assert(32 % L == 0, "L must divide the warp");
     static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
-    static_assert(!BF || STAGE / 8 < 65536, "bf16 entry offsets are 16-bit multiples of 8 bytes");
     static_assert(LANE_BYTES == 8 || LANE_BYTES == 16 || LANE_BYTES == 32, "8, 16 or 32 bytes per lane");
     static_assert(NT <= 256, "TMA box width");
+    static_assert(!BF || ADDR || STAGE / 8 < 65536, "packed bf16 offsets are 16-bit multiples of 8 bytes");
 };
 
 // Output column (within the strip) of element v of lane l.  8-byte lanes own
@@ -106,6 +112,7 @@ __global__ void __launch_bounds__(W * 32, MB)
     using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
     constexpr int NCH = C_::NCH, NW = C_::NW;
     constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, ENTRY = C_::ENTRY;
+    constexpr bool ADDR = C_::ADDR;
 
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
@@ -204,7 +211,9 @@ __global__ void __launch_bounds__(W * 32, MB)
         const int k0 = (c_lo + j) * KC;
         const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs);
         if (!ok) kr[2] = 1;
-        const uint32_t stage = smem_addr(stages + s * STAGE) + l * (NCH ? 16 : 8);
+        const uint32_t stage0 = smem_addr(stages + s * STAGE);
+        const uint32_t lane_off = l * (NCH ? 16 : 8);
+        const uint32_t stage = stage0 + lane_off;
         if (ok) {
 #pragma unroll
             for (int i = 0; i < R; ++i) {
@@ -236,7 +245,10 @@ __global__ void __launch_bounds__(W * 32, MB)
                     if (lane < npad) {
                         const bool live = lane < n;
                         const uint32_t off = live ? (uint32_t)(col - k0) * PITCH : 0u;
-                        if constexpr (BF) {
+                        if constexpr (ADDR) {
+                            reinterpret_cast<uint32_t*>(wl)[lane] = stage0 + off;
+                            reinterpret_cast<uint16_t*>(wl + 128)[lane] = live ? (uint16_t)val : (uint16_t)0;
+                        } else if constexpr (BF) {
                             reinterpret_cast<uint32_t*>(wl)[lane] = live ? ((off >> 3) | (val << 16)) : 0u;
                         } else {
                             reinterpret_cast<uint2*>(wl)[lane] = live ? make_uint2(off, val) : make_uint2(0u, 0u);
@@ -245,17 +257,18 @@ __global__ void __launch_bounds__(W * 32, MB)
                     __syncwarp();
                     const int q = npad / G;  // steps of each group
                     const int q4 = q & ~3;
-                    const uint32_t gl = wl_addr + g * q * ENTRY;
-                    // The lane's words of the staged B row at byte offset off.
-                    auto load_b = [&](uint32_t off, uint32_t (&w)[NW]) {
+                    const uint32_t gl = wl_addr + g * q * (ADDR ? 4 : ENTRY);  // ADDR: addresses
+                    const uint32_t gv = wl_addr + 128 + g * q * 2;             // ADDR: values
+                    // The lane's words of the staged B row whose lane slice starts at p.
+                    auto load_b = [&](uint32_t p, uint32_t (&w)[NW]) {
                         if constexpr (NCH == 0) {
-                            const uint2 b = lds64(stage + off);
+                            const uint2 b = lds64(p);
                             w[0] = b.x;
                             w[1] = b.y;
                         } else {
 #pragma unroll
                             for (int c = 0; c < NCH; ++c) {
-                                const uint4 b = lds128(stage + off + c * L * 16);
+                                const uint4 b = lds128(p + c * L * 16);
                                 w[4 * c] = b.x;
                                 w[4 * c + 1] = b.y;
                                 w[4 * c + 2] = b.z;
@@ -263,11 +276,10 @@ __global__ void __launch_bounds__(W * 32, MB)
                             }
                         }
                     };
-                    // One bf16 step: entry e = (stage offset / 8) | value << 16.
-                    auto step_bf16 = [&](uint32_t e) {
+                    // One bf16 step: staged row at shared address ad, value av.
+                    auto step_bf16 = [&](uint32_t ad, uint16_t av) {
                         uint32_t w[NW];
-                        load_b((e & 0xffffu) << 3, w);
-                        const uint16_t av = hi16(e);
+                        load_b(ad + lane_off, w);
 #pragma unroll
                         for (int q = 0; q < NW; ++q) {
                             acc[i][2 * q] = fma_bf16(av, lo16(w[q]), acc[i][2 * q]);
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(W * 32, MB)
                     // One fp32 step: staged row at byte offset off, value bits av.
                     auto step_f32 = [&](uint32_t off, uint32_t av) {
                         uint32_t w[NW];
-                        load_b(off, w);
+                        load_b(stage + off, w);
                         const float x = __uint_as_float(av);
                         const float2 a2 = make_float2(x, x);
 #pragma unroll
@@ -291,12 +303,19 @@ __global__ void __launch_bounds__(W * 32, MB)
 #pragma unroll 1
 #pragma unroll 1
                     for (int t = 0; t < q4; t += 4) {
-                        if constexpr (BF) {
+                        if constexpr (ADDR) {
+                            const uint4 ad = lds128(gl + t * 4);
+                            const uint2 av = lds64(gv + t * 2);
+                            step_bf16(ad.x, lo16(av.x));
+                            step_bf16(ad.y, hi16(av.x));
+                            step_bf16(ad.z, lo16(av.y));
+                            step_bf16(ad.w, hi16(av.y));
+                        } else if constexpr (BF) {
                             const uint4 e = lds128(gl + t * 4);
-                            step_bf16(e.x);
-                            step_bf16(e.y);
-                            step_bf16(e.z);
-                            step_bf16(e.w);
+                            step_bf16(stage0 + ((e.x & 0xffffu) << 3), hi16(e.x));
+                            step_bf16(stage0 + ((e.y & 0xffffu) << 3), hi16(e.y));
+                            step_bf16(stage0 + ((e.z & 0xffffu) << 3), hi16(e.z));
+                            step_bf16(stage0 + ((e.w & 0xffffu) << 3), hi16(e.w));
                         } else {
                             const uint4 e01 = lds128(gl + t * 8);
                             const uint4 e23 = lds128(gl + t * 8 + 16);
@@ -308,8 +327,11 @@ __global__ void __launch_bounds__(W * 32, MB)
                     }
 #pragma unroll 1
                     for (int t = q4; t < q; ++t) {  // 0-3 remaining steps (G == 1 only)
-                        if constexpr (BF) {
-                            step_bf16(lds32(gl + t * 4));
+                        if constexpr (ADDR) {
+                            step_bf16(lds32(gl + t * 4), lds16(gv + t * 2));
+                        } else if constexpr (BF) {
+                            const uint32_t e = lds32(gl + t * 4);
+                            step_bf16(stage0 + ((e & 0xffffu) << 3), hi16(e));
                         } else {
                             const uint2 e = lds64(gl + t * 8);
                             step_f32(e.x, e.y);
