@@ -425,18 +425,29 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+# Source files each timed operation's kernels are built from.
+KERNEL_SOURCES = {
+    "spmm": ("usm_spmm.cu", "usm_device.cuh", "usm_internal.h"),
+    "sddmm": ("usm_sddmm.cu", "usm_device.cuh", "usm_internal.h"),
+}
+
+
+def kernel_source_hash(op):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES["spmm" if op.startswith("spmm") else "sddmm"]:
+        with open(os.path.join(ROOT, "unstructured_sparse_matmul_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(label):
     """DRAM bytes per launch from the committed ncu summary for this launch,
-    if it was captured on the current kernel sources (else None)."""
+    if it was captured on the current sources of its kernels (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    import hashlib
-    h = hashlib.sha256()
-    for f in sorted(os.listdir(os.path.join(ROOT, "unstructured_sparse_matmul_gb300", "csrc"))):
-        with open(os.path.join(ROOT, "unstructured_sparse_matmul_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    src = h.hexdigest()[:16]
+    src = kernel_source_hash(label.split("_")[0])
     for line in open(path):
         parts = line.split()
         if len(parts) == 3 and parts[0] == label and parts[2] == src:

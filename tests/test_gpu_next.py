@@ -117,6 +117,44 @@ def test_sddmm_general_matches_specialised_form(usm):
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("scale", [False, True])
+@pytest.mark.parametrize("nnz_mod4", [0, 3])
+def test_sddmm_strip_sum_paths(usm, dtype, scale, nnz_mod4):
+    """D = 300 spans several column strips, whose partials a second kernel
+    adds: four nonzeros at a time when nnz is a multiple of 4 and every array
+    is aligned, else one at a time (an output starting one element into its
+    buffer forces that).  Both add the same terms in the same order."""
+    import torch
+    M, K, D = 257, 333, 300
+    rng = np.random.default_rng([nnz_mod4, 16])
+    lengths = rng.integers(0, 40, M)
+    lengths[-1] += (nnz_mod4 - int(lengths.sum())) % 4
+    csr = W.random_csr(17, M, K, 0.0, dtype=dtype, lengths=lengths)
+    assert csr.nnz % 4 == nnz_mod4
+    X, Y = W.dense(rng, M, D, 1.0, dtype), W.dense(rng, K, D, 1.0, dtype)
+    ro, ci, vals = csr_dev(csr)
+    nnz = csr.nnz
+    outs = {}
+    for odt in (torch.float32, torch.bfloat16):
+        for offset in (0, 1):
+            buf = torch.full((nnz + 8,), 7.0, dtype=odt, device="cuda")
+            usm.sddmm_general(ro, ci, dev(X, dtype), dev(Y, dtype), values=vals if scale else None,
+                              out=buf[offset:offset + nnz])
+            assert (buf[:offset] == 7).all() and (buf[offset + nnz:] == 7).all()
+            outs[odt, offset] = buf[offset:offset + nnz]
+    f32 = outs[torch.float32, 0]
+    assert torch.equal(f32, outs[torch.float32, 1])
+    for offset in (0, 1):  # bf16 output: the fp32 result rounded to nearest even
+        assert torch.equal(outs[torch.bfloat16, offset], f32.to(torch.bfloat16))
+    a = oracle.widen(csr.values, dtype)
+    ref = oracle.sddmm_general(M, K, csr.row_offsets, csr.col_indices, a, scale, oracle.widen(X, dtype),
+                               oracle.widen(Y, dtype), True)
+    S = oracle.sddmm_error_scale(M, K, csr.row_offsets, csr.col_indices, oracle.widen(X, dtype),
+                                 oracle.widen(Y, dtype)) * (np.abs(a) if scale else 1.0)
+    assert_within(host(f32), ref, S, TOL[dtype], f"strip sum scale={scale} nnz%4={nnz_mod4}")
+
+
 # ---------------------------------------------------------------------------
 # f4: row softmax and the attention chain with it
 # ---------------------------------------------------------------------------

@@ -355,6 +355,47 @@ __global__ void sddmm_strip_sum_kernel(const float* __restrict__ part, long long
     }
 }
 
+// The same sum four nonzeros at a time with 16-byte loads of every strip's
+// partials (nnz a multiple of 4, partials, out and scale aligned to the
+// vector): several loads in flight per thread instead of one.
+__global__ void sddmm_strip_sum4_kernel(const float4* __restrict__ part, long long n4, int nstrips, void* out,
+                                        int out_bf16, const void* scale, int scale_bf16) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+         i += (long long)gridDim.x * blockDim.x) {
+        float4 s = __ldcs(part + i);
+#pragma unroll 4
+        for (int k = 1; k < nstrips; ++k) {
+            const float4 v = __ldcs(part + (long long)k * n4 + i);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        if (scale) {
+            if (scale_bf16) {
+                const uint2 b = __ldg(reinterpret_cast<const uint2*>(scale) + i);
+                s.x *= __uint_as_float(b.x << 16);
+                s.y *= __uint_as_float(b.x & 0xffff0000u);
+                s.z *= __uint_as_float(b.y << 16);
+                s.w *= __uint_as_float(b.y & 0xffff0000u);
+            } else {
+                const float4 c = __ldg(reinterpret_cast<const float4*>(scale) + i);
+                s.x *= c.x;
+                s.y *= c.y;
+                s.z *= c.z;
+                s.w *= c.w;
+            }
+        }
+        if (out_bf16) {
+            const uint32_t lo = (uint32_t)f32_to_bf16_rne(s.x) | ((uint32_t)f32_to_bf16_rne(s.y) << 16);
+            const uint32_t hi = (uint32_t)f32_to_bf16_rne(s.z) | ((uint32_t)f32_to_bf16_rne(s.w) << 16);
+            reinterpret_cast<uint2*>(out)[i] = make_uint2(lo, hi);
+        } else {
+            reinterpret_cast<float4*>(out)[i] = s;
+        }
+    }
+}
+
 __global__ void fill_out_kernel(void* out, long long n, int bf16) {
     for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n;
          p += (long long)gridDim.x * blockDim.x) {
@@ -417,18 +458,29 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);
     if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
     if (nstrips > 1) {
-        long long blocks = ((long long)a.nnz + 255) / 256;
+        const size_t ob = a.out_bf16 ? 8 : 16, sb = a.scale_bf16 ? 8 : 16;
+        const bool vec = a.nnz % 4 == 0 && (uintptr_t)ws % 16 == 0 && (uintptr_t)final_out % ob == 0 &&
+                         (a.scale == nullptr || (uintptr_t)a.scale % sb == 0);
+        const long long items = vec ? a.nnz / 4 : a.nnz;
+        long long blocks = (items + 255) / 256;
         if (blocks > 8 * sms) blocks = 8 * sms;
-        sddmm_strip_sum_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz,
-                                                                nstrips, final_out, a.out_bf16, a.scale,
-                                                                a.scale_bf16);
+        if (vec)
+            sddmm_strip_sum4_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float4*>(ws), items,
+                                                                     nstrips, final_out, a.out_bf16, a.scale,
+                                                                     a.scale_bf16);
+        else
+            sddmm_strip_sum_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz,
+                                                                    nstrips, final_out, a.out_bf16, a.scale,
+                                                                    a.scale_bf16);
         if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
     }
     return USM_OK;
 }
 
 // Strip width by element type and D: fp32 strips are 128 wide (8 lanes x 16
-// values), bf16 strips 128 wide, or 64 when D ≤ 64.
+// values), bf16 strips 128 wide, or 64 when D ≤ 64.  256-wide strips (half
+// the partials) measured 3-7% faster at 70% sparsity on the FFN shapes but
+// 7-24% slower at 90-95%.
 int strip_width(int D, bool bf16) { return (bf16 && D <= 64) ? 64 : 128; }
 
 }  // namespace
