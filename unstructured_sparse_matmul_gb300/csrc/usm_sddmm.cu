@@ -29,9 +29,15 @@
 //   to the caller's workspace and a second kernel adds the strips in order:
 //   no atomics, results are bit-reproducible.
 #include <climits>
+#include <cstdlib>
 
 #include "usm_device.cuh"
 #include "usm_internal.h"
+
+// Most K splits per tile the launch model may choose (1 turns splitting off).
+#ifndef USM_SDDMM_MAX_SPLIT
+#define USM_SDDMM_MAX_SPLIT 16
+#endif
 
 namespace usm {
 namespace {
@@ -198,14 +204,21 @@ __global__ void __launch_bounds__(W * 32, MINB)
         atomicMax(&kr[1], kmax);
     }
     __syncthreads();
+    // The tile's chunks [c_lo, c_lo + nchunks) are split into gridDim.z
+    // contiguous ranges, one per CTA on z: every nonzero falls in exactly one.
     int c_lo = 0, nchunks = 0;
     {
         const int lo = max(kr[0], 0), hi = min(kr[1], a.K - 1);
         if (kr[1] >= 0 && lo <= hi) {
-            c_lo = lo / KC;
-            nchunks = hi / KC - c_lo + 1;
+            const int per = (hi / KC - lo / KC + 1 + gridDim.z - 1) / gridDim.z;
+            const int first = lo / KC + blockIdx.z * per;
+            c_lo = first;
+            nchunks = max(0, min(hi / KC + 1, first + per) - first);
         }
     }
+    // Later ranges start each row at its first nonzero in range (binary search
+    // of the sorted column indices; lanes < R, overlapping the first copy).
+    const bool later = blockIdx.z > 0 && nchunks > 0;
 
     auto issue = [&](int j) {
         const int s = j % NS;
@@ -220,6 +233,16 @@ __global__ void __launch_bounds__(W * 32, MINB)
     if (threadIdx.x == 0) {
         if (nchunks > 0) issue(0);
         if (NS > 1 && nchunks > 1) issue(1);
+    }
+    if (later && my_end > my_start) {
+        const int k_first = c_lo * KC;
+        int lo = my_start, hi = my_end;  // first position with column >= k_first
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(a.col_indices + mid) < k_first) lo = mid + 1;
+            else hi = mid;
+        }
+        my_start = lo;
     }
 
     int cur = my_start;
@@ -430,31 +453,47 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
         a.out = ws;
         a.out_stride = a.nnz;
     }
-    // Rows per warp from a launch time model: whole waves of CTAs (MINB
-    // resident per SM) × per-CTA work, where a CTA stages every row of its K
-    // span (weighted 2: a staged row costs about two consumed ones) and
-    // consumes R·W mean rows.  Against "R as large as still gives ~4 CTAs per
-    // SM" the FFN SDDMM launches ran up to 38% (fp32) and 32% (bf16) faster,
-    // the attention scores 5%.
+    // Rows per warp R and K splits S from a launch time model fitted to a
+    // sweep of the FFN launches (R ∈ {1..32} × S ∈ {1..16}, fp32 and bf16,
+    // L2 flushed between calls; the choices average 3% above the best pair
+    // per launch, against 7% for R alone).  Time = (CTAs / resident slots, at
+    // least 1, plus one CTA for the tail) × per-CTA work, in units of one
+    // consumed row: staging the CTA's share of the K span (0.6 a row), its
+    // share of R·W mean-length rows, a fixed start-up (3500: first copy,
+    // cursor search, epilogue) and a latency per (row, chunk) that a warp's
+    // R rows pay one after another (220).  Splitting K costs no reduction
+    // (each nonzero belongs to one split); only split counts that give every
+    // split a different chunk range are tried.
     const int sms = sm_count_current_device();
-    const long long slots = (long long)sms * MINB;
+    const double slots = (double)sms * MINB;
     // A block-diagonal schedule (seg_rows < M) is taken to have square blocks.
     const double kspan = (a.seg_rows > 0 && a.seg_rows < a.M) ? (double)min(a.K, a.seg_rows) : (double)a.K;
     const double mean_len = (double)a.nnz / (a.M > 0 ? a.M : 1);
-    int R = 32;
+    const int nch = max(1, (int)((kspan + KC - 1) / KC));
+    int R = 1, S = 1;
     double best = 0.0;
-    for (int r = 32; r >= 1; r >>= 1) {
-        const long long n = schedule_tiles(a.M, a.seg_rows, r * W) * nstrips;
-        const double c = (double)((n + slots - 1) / slots) * (2.0 * kspan + (double)r * W * mean_len);
-        if (r == 32 || c < best) {
-            best = c;
-            R = r;
+    for (int sp = 1; sp <= min(USM_SDDMM_MAX_SPLIT, nch); ++sp) {
+        const int per = (nch + sp - 1) / sp;
+        if ((nch + per - 1) / per != sp) continue;  // same ranges as a smaller count
+        for (int r = 1; r <= 32; r <<= 1) {
+            const double n = (double)schedule_tiles(a.M, a.seg_rows, r * W) * nstrips * sp;
+            const double work = (0.6 * kspan + (double)r * W * mean_len) * per / nch + 3500.0 + 220.0 * per * r;
+            const double c = (fmax(n / slots, 1.0) + 1.0) * work;
+            if (best == 0.0 || c < best) {
+                best = c;
+                R = r;
+                S = sp;
+            }
         }
     }
+#ifdef USM_TUNE_ENV  // tuning builds only: override the model's choice
+    if (const char* e = getenv("USM_SDDMM_R")) R = atoi(e);
+    if (const char* e = getenv("USM_SDDMM_S")) S = atoi(e);
+#endif
     a.rows_per_warp = R;
     const long long tiles = schedule_tiles(a.M, a.seg_rows, R * W);
     if (tiles > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
-    const dim3 grid((unsigned)tiles, nstrips);
+    const dim3 grid((unsigned)tiles, nstrips, S);
     kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);
     if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
     if (nstrips > 1) {

@@ -55,9 +55,14 @@ struct SpmmCfg {
     static constexpr int LANE_BYTES = VEC * ES;    // B bytes per lane per step
     static constexpr int NCH = LANE_BYTES / 16;    // 16-byte loads per lane per step (0: one 8-byte load)
     static constexpr int EPC = 16 / ES;            // elements per 16-byte chunk
-    static constexpr int PITCH = L * LANE_BYTES;   // bytes per staged B row
+    // The stage holds NBOX TMA boxes side by side in memory, each KC rows of
+    // BOX_COLS columns (a box is at most 256 elements wide).
+    static constexpr int BOX_COLS = NT <= 256 ? NT : 256;
+    static constexpr int NBOX = NT / BOX_COLS;
+    static constexpr int PITCH = BOX_COLS * ES;    // bytes per staged row of one box
     static constexpr int NW = LANE_BYTES / 4;      // 32-bit words per lane per step
-    static constexpr int STAGE = KC * PITCH;
+    static constexpr int BOX_BYTES = KC * PITCH;
+    static constexpr int STAGE = NBOX * BOX_BYTES;
     static constexpr int MT = R * W;
     static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
     static constexpr int THREADS = W * 32;
@@ -74,8 +79,12 @@ struct SpmmCfg {
     static_assert(32 % L == 0, "L must divide the warp");
     static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
     static_assert(LANE_BYTES == 8 || LANE_BYTES == 16 || LANE_BYTES == 32, "8, 16 or 32 bytes per lane");
-    static_assert(NT <= 256, "TMA box width");
-    static_assert(!BF || ADDR || STAGE / 8 < 65536, "packed bf16 offsets are 16-bit multiples of 8 bytes");
+    // Byte offset, from a staged row's start in box 0, of 16-byte piece c of
+    // a lane's slice (lane offset excluded): piece c covers bytes
+    // [c·L·16, (c+1)·L·16) of the row, which may lie in a later box.
+    static constexpr int piece_off(int c) { return (c * L * 16) / PITCH * BOX_BYTES + (c * L * 16) % PITCH; }
+    static_assert(NT % BOX_COLS == 0 && (NCH == 0 || PITCH % (L * 16) == 0), "16-byte pieces tile the boxes");
+    static_assert(!BF || ADDR || BOX_BYTES / 8 < 65536, "packed bf16 offsets are 16-bit multiples of 8 bytes");
 };
 
 // Output column (within the strip) of element v of lane l.  8-byte lanes own
@@ -182,9 +191,11 @@ __global__ void __launch_bounds__(W * 32, MB)
         mbar_arrive_expect_tx(bar, STAGE);
         const uint32_t dst = smem_addr(stages + s * STAGE);
 #pragma unroll
-        for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
-            tma_load_2d(dst + b * C_::BOX_ROWS * PITCH, &tmB, n0, (c_lo + j) * KC + b * C_::BOX_ROWS,
-                        bar);
+        for (int x = 0; x < C_::NBOX; ++x)
+#pragma unroll
+            for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
+                tma_load_2d(dst + x * C_::BOX_BYTES + b * C_::BOX_ROWS * PITCH, &tmB, n0 + x * C_::BOX_COLS,
+                            (c_lo + j) * KC + b * C_::BOX_ROWS, bar);
     };
     if (threadIdx.x == 0) {
         if (nchunks > 0) issue(0);
@@ -268,7 +279,7 @@ __global__ void __launch_bounds__(W * 32, MB)
                         } else {
 #pragma unroll
                             for (int c = 0; c < NCH; ++c) {
-                                const uint4 b = lds128(p + c * L * 16);
+                                const uint4 b = lds128(p + C_::piece_off(c));
                                 w[4 * c] = b.x;
                                 w[4 * c + 1] = b.y;
                                 w[4 * c + 2] = b.z;
@@ -427,7 +438,7 @@ template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB>
 int launch_cfg(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
     using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
     CUtensorMap map;
-    if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::NT, C_::BOX_ROWS)) return USM_ERR_CUDA;
+    if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::BOX_COLS, C_::BOX_ROWS)) return USM_ERR_CUDA;
     auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS, MB>;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
@@ -477,7 +488,7 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 // resident per SM) × per-CTA work, where a CTA stages every row of its K span
 // (weighted 2: a staged row costs about two consumed ones) and consumes
 // R·W mean rows.
-template <bool BF, int L, int VEC, int W, int KC, int NS, int MB>
+template <bool BF, int L, int VEC, int W, int KC, int NS, int MB, int RA = 2, int RB = 4>
 int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
     const long long slots = (long long)sm_count_current_device() * MB;
     const int nt = L * VEC;
@@ -488,8 +499,8 @@ int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) 
         const long long n = schedule_tiles(a.M, a.seg_rows, mt) * ((a.N + nt - 1) / nt);
         return (double)((n + slots - 1) / slots) * (2.0 * kspan + mt * mean_len);
     };
-    if (cost(2 * W) < cost(4 * W)) return launch_cfg<BF, L, VEC, 2, W, KC, NS, MB>(a, B, ldb, stream);
-    return launch_cfg<BF, L, VEC, 4, W, KC, NS, MB>(a, B, ldb, stream);
+    if (cost(RA * W) < cost(RB * W)) return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB>(a, B, ldb, stream);
+    return launch_cfg<BF, L, VEC, RB, W, KC, NS, MB>(a, B, ldb, stream);
 }
 
 int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
@@ -501,6 +512,8 @@ int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream
     }
     if (a.N <= 64) return launch_pick<true, 16, 4, W, 384 * F, NS, 2>(a, B, ldb, stream);
     if (a.N <= 128) return launch_pick<true, 32, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
+    // 16 bf16 a lane (512-column strips in two TMA boxes, fewer instructions
+    // per FMA) measured no faster at 70% and 6-25% slower at 90-95%.
     return launch_pick<true, 32, 8, W, 96 * F, NS, 2>(a, B, ldb, stream);
 }
 
