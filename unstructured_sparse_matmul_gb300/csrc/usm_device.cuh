@@ -150,11 +150,12 @@ __device__ __forceinline__ uint16_t lds16(uint32_t addr) {
 // (row tile, slot) in a boustrophedon order: tile t of a block takes
 // positions t, 2T-1-t, 2T+t, ... (T tiles per block), so every tile gets a
 // similar mix of long and short rows, and a tile never spans two blocks.
+// The launcher picks T ≥ ceil(seg / slots per tile), so no tile overflows;
+// more tiles than that hold fewer rows each (to fill the last wave of CTAs).
 // Slots alternate over the warps the same way.  Returns the position in the
 // swizzle, or -1 past the block or the matrix.
-__device__ __forceinline__ long long sched_pos(int tile, int slot, int MT, int seg, int M) {
-    const int T = (seg + MT - 1) / MT;  // tiles per block
-    const int b = tile / T, t = tile - b * T;
+__device__ __forceinline__ long long sched_pos(int tile, int slot, int T, int seg, int M) {
+    const int b = tile / T, t = tile - b * T;  // T: tiles per block
     const long long p = (long long)slot * T + ((slot & 1) ? (T - 1 - t) : t);
     if (p >= seg) return -1;
     const long long m = (long long)b * seg + p;

@@ -20,6 +20,7 @@ struct SpmmArgs {
     float* C;
     long long ldc;
     int* status;
+    int tiles_per_block = 0;  // row tiles per diagonal block (set by the launcher)
 };
 
 struct SddmmArgs {
@@ -37,6 +38,7 @@ struct SddmmArgs {
     int* status;
     const void* scale;   // null, or the mask's values: out[p] is multiplied by scale[p]
     int scale_bf16;      // scale elements are bf16 (else fp32)
+    int tiles_per_block = 0;  // row tiles per diagonal block (set by the launcher)
 };
 
 // Device status word of the current device (null if it cannot be resolved).
@@ -96,6 +98,7 @@ int launch_permute_values(int nnz, const int* perm, const void* values, bool bf1
 inline long long schedule_tiles(int M, int seg, int MT) {
     return (long long)((M + seg - 1) / seg) * ((seg + MT - 1) / MT);
 }
+inline long long block_count(int M, int seg) { return (M + seg - 1) / seg; }
 inline int effective_seg(int M, int seg_rows) { return (seg_rows <= 0 || seg_rows > M) ? M : seg_rows; }
 
 int launch_wait_timeout_selftest(long long limit_ns, int* status, cudaStream_t stream);

@@ -158,7 +158,6 @@ __global__ void __launch_bounds__(W * 32, MINB)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane / L, l = lane % L;
     const int R = a.rows_per_warp;  // ≤ 32
-    const int MT = R * W;
     const int tile = blockIdx.x;
     const int strip = blockIdx.y;
     const int d0 = strip * C_::DT;
@@ -175,7 +174,7 @@ __global__ void __launch_bounds__(W * 32, MINB)
 
     int my_row = -1, my_start = 0, my_end = 0;
     if (lane < R) {
-        const long long m = sched_pos(tile, sched_slot(lane, warp, W), MT, a.seg_rows, a.M);
+        const long long m = sched_pos(tile, sched_slot(lane, warp, W), a.tiles_per_block, a.seg_rows, a.M);
         if (m >= 0) {
             const int r = a.perm ? __ldg(a.perm + m) : (int)m;
             if ((unsigned)r < (unsigned)a.M) {
@@ -491,6 +490,7 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     if (const char* e = getenv("USM_SDDMM_S")) S = atoi(e);
 #endif
     a.rows_per_warp = R;
+    a.tiles_per_block = (a.seg_rows + R * W - 1) / (R * W);
     const long long tiles = schedule_tiles(a.M, a.seg_rows, R * W);
     if (tiles > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)tiles, nstrips, S);
