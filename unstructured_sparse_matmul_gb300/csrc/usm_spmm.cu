@@ -208,10 +208,21 @@ __global__ void __launch_bounds__(W * 32, MB)
         for (int v = 0; v < VEC; ++v) acc[i][v] = 0.f;
 
     int cur = my_start;  // lane i: cursor of row slot i
-    int pcol;
-    uint32_t pval;
-    load_window<BF>(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), lane, pcol,
-                    pval);
+    // PERSIST (one CTA per SM, registers to spare): each row slot keeps a
+    // 32-entry window of its CSR arrays in registers across chunks (lane e
+    // holds entry wb[i] + e), so at high sparsity one window serves several
+    // chunks.  Otherwise (two CTAs per SM, 64 registers) the window of the
+    // next row slot is fetched while the current one computes.
+    constexpr bool PERSIST = MB == 1;
+    constexpr int RW = PERSIST ? R : 1;
+    int wcol[RW];
+    uint32_t wval[RW];
+    int wb[RW];
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+        wb[i] = __shfl_sync(kFullMask, cur, i);
+        load_window<BF>(a, wb[i], __shfl_sync(kFullMask, my_end, i), lane, wcol[i], wval[i]);
+    }
 
     unsigned char* wl = lists + warp * 32 * ENTRY;
     const uint32_t wl_addr = smem_addr(wl);
@@ -229,39 +240,49 @@ __global__ void __launch_bounds__(W * 32, MB)
             for (int i = 0; i < R; ++i) {
                 int rc = __shfl_sync(kFullMask, cur, i);
                 const int re = __shfl_sync(kFullMask, my_end, i);
-                int col = pcol;
-                uint32_t val = pval;
-                if (i + 1 < R)
-                    load_window<BF>(a, __shfl_sync(kFullMask, cur, i + 1),
-                                    __shfl_sync(kFullMask, my_end, i + 1), lane, pcol, pval);
+                int col = wcol[PERSIST ? i : 0];
+                uint32_t val = wval[PERSIST ? i : 0];
+                int base = PERSIST ? wb[i] : rc;  // position of the window's lane 0 (rc - base < 32)
+                if constexpr (!PERSIST) {
+                    if (i + 1 < R) {
+                        wb[0] = __shfl_sync(kFullMask, cur, i + 1);
+                        load_window<BF>(a, wb[0], __shfl_sync(kFullMask, my_end, i + 1), lane, wcol[0], wval[0]);
+                    }
+                }
                 float c4[BF ? 1 : VEC];  // fp32: this window's partial sums (≤ 32 terms)
                 float cc[BF ? 1 : VEC];  // fp32: this chunk segment's windows
 #pragma unroll
                 for (int v = 0; v < (BF ? 1 : VEC); ++v) c4[v] = cc[v] = 0.f;
                 while (true) {
-                    const bool valid = (rc + lane < re) && ((unsigned)(col - k0) < (unsigned)KC);
-                    const unsigned bal = __ballot_sync(kFullMask, valid);
-                    const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);  // valid prefix
+                    // The chunk's entries of this row: a run of the window from
+                    // lane rc - base (columns are sorted).
+                    const int wo = PERSIST ? rc - base : 0;  // without PERSIST the window starts at rc
+                    const bool valid = lane >= wo && (base + lane < re) && ((unsigned)(col - k0) < (unsigned)KC);
+                    const unsigned run = __ballot_sync(kFullMask, valid) >> wo;
+                    const int n = (run == kFullMask) ? 32 : (__ffs(~run) - 1);
                     if (n == 0) break;
-                    // A full window may continue: fetch the next one now so its
-                    // latency overlaps this window's work.
+                    // The window runs out inside this chunk: fetch the next one
+                    // now so its latency overlaps this window's work.
+                    const bool more = wo + n == 32;
                     int ncol = INT_MAX;
                     uint32_t nval = 0;
-                    if (n == 32) load_window<BF>(a, rc + 32, re, lane, ncol, nval);
+                    if (more) load_window<BF>(a, base + 32, re, lane, ncol, nval);
                     // G == 1: exact count (0-3 single steps at the end).  G > 1: each
                     // group's block must start 16-byte aligned for the 128-bit
-                    // entry loads, so pad to a multiple of 4·G.
+                    // entry loads, so pad to a multiple of 4·G.  Lane e writes
+                    // list slot (e - wo) mod 32: every slot below npad is written.
                     const int npad = (G == 1) ? n : (n + 4 * G - 1) / (4 * G) * (4 * G);
-                    if (lane < npad) {
-                        const bool live = lane < n;
+                    const int slot = (lane - wo) & 31;
+                    if (slot < npad) {
+                        const bool live = slot < n;
                         const uint32_t off = live ? (uint32_t)(col - k0) * PITCH : 0u;
                         if constexpr (ADDR) {
-                            reinterpret_cast<uint32_t*>(wl)[lane] = stage0 + off;
-                            reinterpret_cast<uint16_t*>(wl + 128)[lane] = live ? (uint16_t)val : (uint16_t)0;
+                            reinterpret_cast<uint32_t*>(wl)[slot] = stage0 + off;
+                            reinterpret_cast<uint16_t*>(wl + 128)[slot] = live ? (uint16_t)val : (uint16_t)0;
                         } else if constexpr (BF) {
-                            reinterpret_cast<uint32_t*>(wl)[lane] = live ? ((off >> 3) | (val << 16)) : 0u;
+                            reinterpret_cast<uint32_t*>(wl)[slot] = live ? ((off >> 3) | (val << 16)) : 0u;
                         } else {
-                            reinterpret_cast<uint2*>(wl)[lane] = live ? make_uint2(off, val) : make_uint2(0u, 0u);
+                            reinterpret_cast<uint2*>(wl)[slot] = live ? make_uint2(off, val) : make_uint2(0u, 0u);
                         }
                     }
                     __syncwarp();
@@ -356,18 +377,33 @@ __global__ void __launch_bounds__(W * 32, MB)
                         }
                     }
                     rc += n;
-                    if (n < 32) break;
+                    if (!more) break;
                     col = ncol;
                     val = nval;
+                    base += 32;
                 }
                 if constexpr (!BF) {
 #pragma unroll
                     for (int v = 0; v < VEC; ++v) acc[i][v] += cc[v];
                 }
+                if constexpr (PERSIST) {
+                    // Half the window used: refill it from the cursor now; the
+                    // load lands while the other rows and the next chunk's wait
+                    // go by.
+                    if (rc - base >= 16 && rc < re) {
+                        base = rc;
+                        load_window<BF>(a, rc, re, lane, col, val);
+                    }
+                    wcol[i] = col;
+                    wval[i] = val;
+                    wb[i] = base;
+                }
                 if (lane == i) cur = rc;
-                if (i + 1 == R)
-                    load_window<BF>(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0),
-                                    lane, pcol, pval);
+                if constexpr (!PERSIST) {
+                    if (i + 1 == R)
+                        load_window<BF>(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), lane,
+                                        wcol[0], wval[0]);
+                }
             }
         }
         __syncthreads();  // every warp is done with stage s
@@ -476,8 +512,9 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 // latency-bound and run two CTAs per SM (≤ 64 registers, 96 KB of stage
 // each); fp32 steps are bound by shared-memory bandwidth and run one CTA per
 // SM with up to 128 registers and one 192 KB stage (N > 128: KC = 192 rows
-// of 1 KB; N ≤ 128: 384 rows of 512 B): taller chunks halve the per-(row,
-// chunk) work and more rows per CTA share each staged row.  Measured against
+// of 1 KB; N ≤ 128: 384 rows of 512 B; N ≤ 64: 768 of 256 B): taller chunks
+// halve the per-(row, chunk) work and more rows per CTA share each staged
+// row, and row slots keep their CSR windows across chunks.  Measured against
 // two CTAs per SM: FFN fp32 SpMM 3-12% faster, LSTM (N = 128) 5% faster at
 // 50% sparsity up to 39% at 98%.  One tall stage (the default) against two
 // stages of half the height: the FFN step took 7.69 against 8.90 ms.
@@ -528,7 +565,7 @@ int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) 
 int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
     if (!bf16) {
-        if (a.N <= 64) return launch_pick<false, 16, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
+        if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1>(a, B, ldb, stream);
         if (a.N <= 128) return launch_pick<false, 32, 4, W, 192 * F, NS, 1>(a, B, ldb, stream);
         return launch_pick<false, 32, 8, W, 96 * F, NS, 1>(a, B, ldb, stream);
     }
