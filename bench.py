@@ -75,7 +75,11 @@ WORKLOADS = {
     "lstm": "LSTM-sized sweep, fp32: A 8192x4096 at 50/60/70/80/90/95/98%, B 4096x128, SpMM only",
     "resnet": "ResNet-50-like 1x1 conv, fp32: A 512x2048 at 80%, B 2048x3136 SpMM and SDDMM weight-gradient "
               "(X 512x3136, Y 2048x3136); L2 flushed before every step",
+    "tiny": "tiny parity config, fp32: A 256x256 at 90%, B/X/Y 256x64, SpMM and SDDMM; launch-bound, so each "
+            "call is timed as a CUDA graph of 100 calls (warm L2: the whole problem is 0.2 MB)",
 }
+GRAPH_CALLS = 100  # calls per CUDA graph for the launch-bound workloads
+GRAPHED = {"tiny"}
 # Workloads whose operands fit in L2: a 256 MB buffer is written before every
 # step and throughput comes from the launches' own events.
 FLUSH_L2 = {"resnet"}
@@ -91,6 +95,8 @@ def problems(only=None, workload="ffn"):
         return [p for p in (W.lstm(s) for s in W.LSTM_SPARSITIES) if keep(p)]
     if workload == "resnet":
         return [p for p in [W.resnet()] if keep(p)]
+    if workload == "tiny":
+        return [W.tiny()]
     out = []
     for dtype in ("f32", "bf16"):
         for (M, K) in W.FFN_SHAPES:
@@ -351,7 +357,31 @@ def run_ours(args, rank, world, local_rank):
     per_launch_ms = {label: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
                      for i, (label, _, _) in enumerate(launches)}
 
-    if flush is not None:  # the flush is not the path's work: time the launches alone
+    if wl in GRAPHED:
+        # Launch-bound: each call's time from a CUDA graph of GRAPH_CALLS calls
+        # replayed `steps` times, so launch gaps do not count.
+        side = torch.cuda.Stream(device=dev)
+        for label, op, d in launches:
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    run_one(op, d)
+            stream.wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(GRAPH_CALLS):
+                    run_one(op, d)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            graph.replay()
+            g0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            g1.record(stream)
+            torch.cuda.synchronize()
+            per_launch_ms[label] = g0.elapsed_time(g1) / (args.steps * GRAPH_CALLS)
+        if usm.poll_status() != 0:
+            raise RuntimeError("device status word set during the graph replays")
+    if flush is not None or wl in GRAPHED:  # time the launches alone
         elapsed_ms = sum(per_launch_ms.values()) * args.steps
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
@@ -400,7 +430,9 @@ def run_ours(args, rank, world, local_rank):
                    + (f" [only {args.only}]" if args.only else ""),
                    "launches_per_step": len(launches),
                    "l2": ("L2 flushed (256 MB written) before every step; value from the launches' events"
-                          if flush is not None else "inputs larger than L2: each step's operands exceed 129 MB"),
+                          if flush is not None else
+                          f"warm L2 (0.2 MB problem); each call timed in a CUDA graph of {GRAPH_CALLS} calls"
+                          if wl in GRAPHED else "inputs larger than L2: each step's operands exceed 129 MB"),
                    "swizzle": "row swizzle built once per pattern before timing",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm_alg_gbs": round(step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9, 1),
@@ -415,7 +447,8 @@ def run_ours(args, rank, world, local_rank):
                                                  "element per useful FMA"}},
         "setup": {"row_swizzle_ms_all_patterns": round(swz_ms, 4), "patterns": len(items)},
         "per_launch": rows,
-        "gpu_launches": sum(kernels_per_launch[label] for label, _, _ in launches) * args.steps,
+        "gpu_launches": sum(kernels_per_launch[label] for label, _, _ in launches) * args.steps
+                        * (GRAPH_CALLS if wl in GRAPHED else 1),
         "clocks": clocks,
     }
     if e2e is not None:
