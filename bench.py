@@ -570,9 +570,9 @@ def run_e2e(args, usm, torch, dev, launches, step_flops):
 # ---------------------------------------------------------------------------
 # CPU oracle arm (cpu_baseline / --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_sample_pass(probs, frac):
-    """Run the oracle on a row sample of every launch of one step; returns
-    (flops done, seconds)."""
+def oracle_sample_pass(probs, frac, nthreads=0):
+    """Run the oracle on a row sample of every launch of one step on
+    `nthreads` host threads (0: all); returns (flops done, seconds)."""
     import oracle
     flops, secs = 0.0, 0.0
     for p in probs:
@@ -585,8 +585,8 @@ def oracle_sample_pass(probs, frac):
         X = oracle.widen(p.X, p.dtype)[rows]
         Y = oracle.widen(p.Y, p.dtype)
         t0 = time.perf_counter()
-        oracle.spmm(rows.size, csr.K, ro, ci, vals, B)
-        oracle.sddmm(rows.size, csr.K, ro, ci, X, Y)
+        oracle.spmm(rows.size, csr.K, ro, ci, vals, B, nthreads)
+        oracle.sddmm(rows.size, csr.K, ro, ci, X, Y, nthreads)
         secs += time.perf_counter() - t0
         flops += 2 * 2.0 * pos.size * N_FFN
     return flops, secs
@@ -602,10 +602,14 @@ def cpu_baseline(frac, only=None, passes=2):
         f, t = oracle_sample_pass(probs, frac)
         flops += f
         secs += t
+    # The same on one core, on a sample 1/16 the size (about as long).
+    f1, t1 = oracle_sample_pass(probs, frac / 16, nthreads=1)
     return {"value": round(flops / secs / 1e9, 3), "unit": "GFLOP/s", "cores": oracle.max_threads(),
             "kind": "oracle",
             "sample": f"{passes} passes over every launch of one step on a {frac:.4g} row sample "
-                      f"(rows evenly spaced): {flops / 1e9:.1f} GFLOP in {secs:.1f} s"}
+                      f"(rows evenly spaced): {flops / 1e9:.1f} GFLOP in {secs:.1f} s",
+            "value_1core": round(f1 / t1 / 1e9, 3),
+            "sample_1core": f"one pass on a {frac / 16:.4g} row sample: {f1 / 1e9:.1f} GFLOP in {t1:.1f} s"}
 
 
 def run_reference(args, rank, world):
