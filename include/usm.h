@@ -270,6 +270,29 @@ const char *usm_status_string(int status);
  */
 int usm_selftest_wait_timeout(long long limit_ns, void *stream);
 
+/*
+ * usm_set_schedule_override — for tests and tuning (the pages have no
+ * counterpart): forces the launch shape of later csr_spmm and csr_sddmm
+ * calls (including the general and static-scratch forms) in this process.
+ * A field of 0 keeps the library's own choice.
+ *   rows_per_warp    row slots per warp, one of 1, 2, 4, 8, 16, 32
+ *                    (csr_spmm has kernels for 2 and 4 only: a forced value
+ *                    it has none for makes the call return
+ *                    USM_ERR_UNSUPPORTED);
+ *   tiles_per_block  row tiles per diagonal block of the schedule (raised to
+ *                    the fewest that hold a block, if below);
+ *   k_splits         csr_sddmm: ranges of K chunks, one CTA each (split
+ *                    counts above the chunk count leave CTAs idle);
+ *                    csr_spmm accepts only 0 or 1.
+ * Results do not depend on the schedule: an SDDMM output adds the same
+ * terms in the same order under every schedule, and so does an SpMM output
+ * under every schedule of one element type and strip width.  The setting is
+ * process-wide and not ordered with calls issued concurrently on other
+ * threads.  Returns USM_ERR_INVALID_ARG (setting unchanged) for a value
+ * outside these sets.
+ */
+int usm_set_schedule_override(int rows_per_warp, int tiles_per_block, int k_splits);
+
 #ifdef __cplusplus
 }
 #endif

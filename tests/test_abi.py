@@ -163,3 +163,15 @@ def test_binding_refuses_without_gpu():
         pytest.skip("a GPU is present")
     with pytest.raises(RuntimeError, match="no CUDA device"):
         usm.spmm(None, None, None, None)
+
+
+def test_schedule_override_validation(lib):
+    f = lib.usm_set_schedule_override
+    INVALID = -1
+    try:
+        for bad in [(3, 0, 0), (64, 0, 0), (-1, 0, 0), (0, -1, 0), (0, 0, -1), (0, 0, 65536)]:
+            assert f(*bad) == INVALID, bad
+        for good in [(0, 0, 0), (1, 0, 0), (32, 5, 7), (4, 0, 65535), (16, 100000, 1)]:
+            assert f(*good) == 0, good
+    finally:
+        assert f(0, 0, 0) == 0

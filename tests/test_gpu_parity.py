@@ -385,3 +385,71 @@ def test_scheduler_does_not_change_bits(usm, dtype):
     assert_within(Cs[0], ref, S, TOL[dtype], "block-diagonal spmm")
     ref, S, _ = oracle_sddmm(csr, X, B, dtype)
     assert_within(Ss[0], ref, S, TOL[dtype], "block-diagonal sddmm")
+
+
+@pytest.fixture
+def schedule(usm):
+    """Sets the launch-shape override for a test and always clears it."""
+    yield usm.set_schedule_override
+    usm.set_schedule_override(0, 0, 0)
+
+
+SDDMM_SCHEDULES = [(0, 0, 0), (1, 0, 1), (2, 0, 5), (8, 0, 3), (32, 0, 1), (4, 40, 2), (16, 0, 11), (1, 0, 16)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("seg", [0, 350])
+def test_sddmm_schedules_do_not_change_bits(usm, schedule, dtype, seg):
+    """Rows per warp, tiles per block and K splits change which CTA computes
+    a nonzero, never the order of its terms: the outputs are bit-identical
+    (D = 300 spans three strips; seg = 350 makes a block-diagonal schedule)."""
+    M, K, D = 700, 3000, 300
+    csr = W.random_csr([M, K, 140], M, K, 0.1, dtype=dtype)
+    rng = np.random.default_rng(141)
+    X, Y = W.dense(rng, M, D, 1.0, dtype), W.dense(rng, K, D, 1.0, dtype)
+    rod, cid = dev(csr.row_offsets), dev(csr.col_indices)
+    Xd, Yd = dev(X, dtype), dev(Y, dtype)
+    perm = usm.row_swizzle(rod, K, seg)
+    outs = []
+    for r, t, s in SDDMM_SCHEDULES:
+        schedule(r, t, s)
+        outs.append(host(usm.sddmm(rod, cid, Xd, Yd, row_swizzle=perm, seg_rows=seg)))
+    for (r, t, s), o in zip(SDDMM_SCHEDULES[1:], outs[1:]):
+        assert np.array_equal(o, outs[0]), (r, t, s)
+    ref, S, _ = oracle_sddmm(csr, X, Y, dtype)
+    assert_within(outs[0], ref, S, TOL[dtype], "sddmm under forced schedules")
+
+
+SPMM_SCHEDULES = [(0, 0, 0), (2, 0, 0), (4, 0, 0), (2, 50, 0), (4, 7, 0), (0, 44, 1)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [64, 300])
+@pytest.mark.parametrize("seg", [0, 350])
+def test_spmm_schedules_do_not_change_bits(usm, schedule, dtype, N, seg):
+    """Rows per warp and tiles per block move rows between CTAs and warps,
+    not the order of a row's terms: the outputs are bit-identical."""
+    M, K = 700, 3000
+    csr = W.random_csr([M, K, N, 142], M, K, 0.1, dtype=dtype)
+    B = W.dense(np.random.default_rng(143), K, N, 1.0, dtype)
+    rod, cid, vd = csr_dev(csr)
+    Bd = dev(B, dtype)
+    perm = usm.row_swizzle(rod, K, seg)
+    outs = []
+    for r, t, s in SPMM_SCHEDULES:
+        schedule(r, t, s)
+        outs.append(host(usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm, seg_rows=seg)))
+    for (r, t, s), c in zip(SPMM_SCHEDULES[1:], outs[1:]):
+        assert np.array_equal(c, outs[0]), (r, t, s)
+    ref, S = oracle_spmm(csr, B, dtype)
+    assert_within(outs[0], ref, S, TOL[dtype], "spmm under forced schedules")
+
+
+def test_spmm_rejects_schedules_it_has_no_kernel_for(usm, schedule):
+    csr = W.random_csr(144, 100, 200, 0.1)
+    rod, cid, vd = csr_dev(csr)
+    Bd = dev(W.dense(np.random.default_rng(145), 200, 64))
+    for r, t, s in [(8, 0, 0), (1, 0, 0), (0, 0, 3)]:
+        schedule(r, t, s)
+        with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+            usm.spmm(rod, cid, vd, Bd, K=200)

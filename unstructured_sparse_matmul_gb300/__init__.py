@@ -36,6 +36,7 @@ SIGNATURES = {
     "usm_poll_status": (_i, [_vp]),
     "usm_status_string": (ctypes.c_char_p, [_i]),
     "usm_selftest_wait_timeout": (_i, [_ll, _vp]),
+    "usm_set_schedule_override": (_i, [_i, _i, _i]),
     "csr_sddmm_static_scratch": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _vp, _i, _i, _vp]),
     "csr_transpose_workspace_bytes": (_sz, [_i, _i, _i]),
     "csr_sddmm_general_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
@@ -309,6 +310,12 @@ def csr_permute_values(perm, values, out=None, stream=None):
 
 def poll_status(stream=None) -> int:
     return int(load().usm_poll_status(_stream(stream)))
+
+
+def set_schedule_override(rows_per_warp: int = 0, tiles_per_block: int = 0, k_splits: int = 0) -> None:
+    """Force the launch shape of later SpMM/SDDMM calls (0 = the library's
+    choice); see usm_set_schedule_override."""
+    _check("usm_set_schedule_override", load().usm_set_schedule_override(rows_per_warp, tiles_per_block, k_splits))
 
 
 def status_string(code: int) -> str:

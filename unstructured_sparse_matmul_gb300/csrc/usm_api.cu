@@ -94,6 +94,17 @@ int launch_wait_timeout_selftest(long long limit_ns, int* status, cudaStream_t s
 
 using namespace usm;
 
+namespace {
+std::atomic<int> g_override_rows{0}, g_override_tiles{0}, g_override_splits{0};
+}  // namespace
+
+namespace usm {
+ScheduleOverride schedule_override() {
+    return {g_override_rows.load(std::memory_order_relaxed), g_override_tiles.load(std::memory_order_relaxed),
+            g_override_splits.load(std::memory_order_relaxed)};
+}
+}  // namespace usm
+
 extern "C" {
 
 int csr_spmm(int M, int K, int N, int nnz, const int* row_offsets, const int* col_indices,
@@ -289,6 +300,15 @@ const char* usm_status_string(int status) {
         case USM_ERR_WORKSPACE: return "USM_ERR_WORKSPACE";
         default: return "USM_UNKNOWN_STATUS";
     }
+}
+
+int usm_set_schedule_override(int rows_per_warp, int tiles_per_block, int k_splits) {
+    const bool r_ok = rows_per_warp == 0 || (rows_per_warp <= 32 && (rows_per_warp & (rows_per_warp - 1)) == 0);
+    if (!r_ok || tiles_per_block < 0 || k_splits < 0 || k_splits > 65535) return USM_ERR_INVALID_ARG;
+    g_override_rows.store(rows_per_warp, std::memory_order_relaxed);
+    g_override_tiles.store(tiles_per_block, std::memory_order_relaxed);
+    g_override_splits.store(k_splits, std::memory_order_relaxed);
+    return USM_OK;
 }
 
 int usm_selftest_wait_timeout(long long limit_ns, void* stream) {

@@ -103,4 +103,10 @@ inline int effective_seg(int M, int seg_rows) { return (seg_rows <= 0 || seg_row
 
 int launch_wait_timeout_selftest(long long limit_ns, int* status, cudaStream_t stream);
 
+// Launch shape forced by usm_set_schedule_override (0: the library's choice).
+struct ScheduleOverride {
+    int rows_per_warp, tiles_per_block, k_splits;
+};
+ScheduleOverride schedule_override();
+
 }  // namespace usm

@@ -29,7 +29,6 @@
 //   to the caller's workspace and a second kernel adds the strips in order:
 //   no atomics, results are bit-reproducible.
 #include <climits>
-#include <cstdlib>
 
 #include "usm_device.cuh"
 #include "usm_internal.h"
@@ -485,13 +484,12 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
             }
         }
     }
-#ifdef USM_TUNE_ENV  // tuning builds only: override the model's choice
-    if (const char* e = getenv("USM_SDDMM_R")) R = atoi(e);
-    if (const char* e = getenv("USM_SDDMM_S")) S = atoi(e);
-#endif
+    const ScheduleOverride ov = schedule_override();
+    if (ov.rows_per_warp > 0) R = ov.rows_per_warp;
+    if (ov.k_splits > 0) S = ov.k_splits;
     a.rows_per_warp = R;
-    a.tiles_per_block = (a.seg_rows + R * W - 1) / (R * W);
-    const long long tiles = schedule_tiles(a.M, a.seg_rows, R * W);
+    a.tiles_per_block = max((a.seg_rows + R * W - 1) / (R * W), ov.tiles_per_block);
+    const long long tiles = block_count(a.M, a.seg_rows) * a.tiles_per_block;
     if (tiles > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)tiles, nstrips, S);
     kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);

@@ -555,10 +555,19 @@ int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) 
         const double sm = std::ceil(n / slots) * MB * (2.0 * kspan + (double)a.seg_rows / t * mean_len);
         return fmax(sm, n * kspan * 5.0 / sms);
     };
-    const int ta0 = (a.seg_rows + RA * W - 1) / (RA * W), ta1 = fill(RA * W);
-    const int tb0 = (a.seg_rows + RB * W - 1) / (RB * W), tb1 = fill(RB * W);
-    const int ta = cost(ta1) < cost(ta0) ? ta1 : ta0, tb = cost(tb1) < cost(tb0) ? tb1 : tb0;
-    if (cost(ta) < cost(tb)) return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB>(a, ta, B, ldb, stream);
+    const ScheduleOverride ov = schedule_override();
+    if (ov.k_splits > 1) return USM_ERR_UNSUPPORTED;
+    auto tiles = [&](int r) {  // the model's tile count for R = r, or the forced one
+        const int t0 = (a.seg_rows + r * W - 1) / (r * W), t1 = fill(r * W);
+        if (ov.tiles_per_block > 0) return max(t0, ov.tiles_per_block);
+        return cost(t1) < cost(t0) ? t1 : t0;
+    };
+    const int ta = tiles(RA), tb = tiles(RB);
+    bool use_a = cost(ta) < cost(tb);
+    if (ov.rows_per_warp == RA) use_a = true;
+    else if (ov.rows_per_warp == RB) use_a = false;
+    else if (ov.rows_per_warp != 0) return USM_ERR_UNSUPPORTED;
+    if (use_a) return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB>(a, ta, B, ldb, stream);
     return launch_cfg<BF, L, VEC, RB, W, KC, NS, MB>(a, tb, B, ldb, stream);
 }
 
