@@ -458,10 +458,11 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
-# Source files each timed operation's kernels are built from.
+# Device source files each timed operation's kernels are built from (the
+# launch code lives apart, so launch-choice changes keep a capture valid).
 KERNEL_SOURCES = {
-    "spmm": ("usm_spmm.cu", "usm_device.cuh", "usm_internal.h"),
-    "sddmm": ("usm_sddmm.cu", "usm_device.cuh", "usm_internal.h"),
+    "spmm": ("usm_spmm_kernel.cuh", "usm_device.cuh", "usm_args.h"),
+    "sddmm": ("usm_sddmm_kernel.cuh", "usm_device.cuh", "usm_args.h"),
 }
 
 
@@ -482,8 +483,8 @@ def recorded_traffic(label):
         return None
     src = kernel_source_hash(label.split("_")[0])
     for line in open(path):
-        parts = line.split()
-        if len(parts) == 3 and parts[0] == label and parts[2] == src:
+        parts = line.split()  # launch, bytes, [algorithmic bytes,] source hash
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == label and parts[-1] == src:
             return int(parts[1])
     return None
 

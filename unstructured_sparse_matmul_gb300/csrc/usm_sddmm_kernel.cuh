@@ -1,0 +1,446 @@
+// CSR SDDMM for sm_103a: out[p] = X[r]·Y[col_p] on the nonzeros of the mask.
+//
+// "Sparse GPU Kernels for Deep Learning" (Gale et al., SC 2020), summary
+// card, "Interesting ideas" I3: the kernel drops the element-wise scaling by
+// the mask's values and takes the second operand transposed (Y is K×D and
+// the product is X·Yᵀ), the form weight gradients and sparse-attention
+// scores need.  GB300 design:
+//
+// * Tiles.  A CTA owns MT = R·W mask rows (dealt from the row-swizzle order
+//   by the row scheduler, sched_pos; R chosen at launch) and one strip of DT
+//   columns of D.  It walks K in chunks of KC
+//   rows; one thread copies Y[k0:k0+KC, d0:d0+DT] into a shared-memory stage
+//   with TMA (mbarrier, bounded wait) into one tall stage: the tall chunks
+//   halve the per-(row, chunk) work of a double-buffered layout.  bf16 runs
+//   two CTAs per SM with 96 KB each (latency-bound: the two CTAs cover each
+//   other's loads); fp32, bound by shared-memory bandwidth, runs one CTA per
+//   SM with a 192 KB stage and up to 128 registers.
+// * Per (row, chunk) a warp keeps X[r, d0:d0+DT] in registers (fp32), reads
+//   the row's next 32 column indices (coalesced window after its cursor),
+//   keeps the prefix inside the chunk and lists their stage offsets.
+// * Dot products.  Lanes form G = 32/L groups of L lanes; at step t group g
+//   takes list entry t·G+g and each lane multiplies its VV·EPV elements of
+//   the staged Y row with its X elements (f32x2 FMA), leaving one partial per
+//   step.  After L steps the L partials of each lane are reduced across the L
+//   lanes of the group with a transpose-reduction (L-1 shuffles for L
+//   results), so lane l of group g ends up with entry l·G+g's strip sum.
+// * Strips.  With one strip the result goes straight to `out` (fp32 or bf16
+//   rounded to nearest even).  With several, each strip writes fp32 partials
+//   to the caller's workspace and a second kernel adds the strips in order:
+//   no atomics, results are bit-reproducible.
+#pragma once
+
+#include <climits>
+
+#include "usm_device.cuh"
+#include "usm_args.h"
+
+
+namespace usm {
+namespace {
+
+template <bool BF, int L, int VV, int W, int KC, int MINB, int NS>
+struct SddmmCfg {
+    static constexpr int EPV = BF ? 8 : 4;      // elements per 16-byte vector
+    static constexpr int DT = L * VV * EPV;     // D columns per CTA
+    static constexpr int G = 32 / L;
+    static constexpr int PITCH = L * VV * 16;   // bytes per staged Y row
+    static constexpr int STAGE = KC * PITCH;
+    static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
+    static constexpr int THREADS = W * 32;
+    static constexpr int SMEM = NS * STAGE + 64 + W * 32 * 4;
+    static constexpr int XW = VV * 4;           // 32-bit words of X per lane
+    static_assert(G * L == 32, "groups must tile the warp");
+    static_assert(L == 8, "the list layout and reduction assume 8-lane groups");
+    static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
+};
+
+// Scaling by the mask's value at nonzero p (general SDDMM), 1 otherwise.
+__device__ __forceinline__ float scale_at(const void* scale, int scale_bf16, long long p) {
+    if (!scale) return 1.f;
+    if (scale_bf16) return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(scale) + p) << 16);
+    return __ldg(reinterpret_cast<const float*>(scale) + p);
+}
+
+__device__ __forceinline__ int window_col(const SddmmArgs& a, int pos, int end, int lane) {
+    const int p = pos + lane;
+    return p < end ? __ldg(a.col_indices + p) : INT_MAX;
+}
+
+// X[r, d0 + j*L*EPV + l*EPV : +EPV] for j < VV as raw 32-bit words (fp32
+// values, or packed bf16 pairs); zero beyond D or for a missing row.
+template <bool BF, int L, int VV>
+__device__ __forceinline__ void load_x(const SddmmArgs& a, int row, int d0, int l, uint32_t (&xw)[VV * 4]) {
+    constexpr int EPV = BF ? 8 : 4;
+#pragma unroll
+    for (int j = 0; j < VV; ++j) {
+        const int c = d0 + j * L * EPV + l * EPV;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row >= 0) {
+            if (BF) {
+                const unsigned short* x =
+                    reinterpret_cast<const unsigned short*>(a.X) + (long long)row * a.ldx + c;
+                if (c + EPV <= a.D) {
+                    v = __ldg(reinterpret_cast<const uint4*>(x));
+                } else {
+                    uint32_t h[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) h[e] = (c + e < a.D) ? __ldg(x + e) : 0u;
+                    v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                   h[6] | (h[7] << 16));
+                }
+            } else {
+                const float* x = reinterpret_cast<const float*>(a.X) + (long long)row * a.ldx + c;
+                if (c + EPV <= a.D) {
+                    v = __ldg(reinterpret_cast<const uint4*>(x));
+                } else {
+                    uint32_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        h[e] = (c + e < a.D) ? __float_as_uint(__ldg(x + e)) : 0u;
+                    v = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+            }
+        }
+        xw[4 * j + 0] = v.x;
+        xw[4 * j + 1] = v.y;
+        xw[4 * j + 2] = v.z;
+        xw[4 * j + 3] = v.w;
+    }
+}
+
+// Partial dot product of one lane: its X words with the 16-byte vectors of
+// one staged Y row.
+template <bool BF, int L, int VV>
+__device__ __forceinline__ float lane_dot(const uint32_t (&xw)[VV * 4], uint32_t yrow) {
+    if constexpr (BF) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < VV; ++j) {
+            const uint4 y = lds128(yrow + j * L * 16);
+            const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                s0 = fma_bf16(lo16(xw[4 * j + q]), lo16(yw[q]), s0);
+                s1 = fma_bf16(hi16(xw[4 * j + q]), hi16(yw[q]), s1);
+            }
+        }
+        return s0 + s1;
+    } else {
+        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < VV; ++j) {
+            const uint4 y = lds128(yrow + j * L * 16);
+            s2 = __ffma2_rn(make_float2(__uint_as_float(xw[4 * j]), __uint_as_float(xw[4 * j + 1])),
+                            make_float2(__uint_as_float(y.x), __uint_as_float(y.y)), s2);
+            s2 = __ffma2_rn(make_float2(__uint_as_float(xw[4 * j + 2]), __uint_as_float(xw[4 * j + 3])),
+                            make_float2(__uint_as_float(y.z), __uint_as_float(y.w)), s2);
+        }
+        return s2.x + s2.y;
+    }
+}
+
+template <bool BF, int L, int VV, int W, int KC, int MINB, int NS>
+__global__ void __launch_bounds__(W * 32, MINB)
+    sddmm_kernel(const __grid_constant__ CUtensorMap tmY, const SddmmArgs a) {
+    using C_ = SddmmCfg<BF, L, VV, W, KC, MINB, NS>;
+    constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, XW = C_::XW;
+
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* stages = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
+    int* kr = reinterpret_cast<int*>(smem + NS * STAGE + 16);
+    uint32_t* lists = reinterpret_cast<uint32_t*>(smem + NS * STAGE + 64);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / L, l = lane % L;
+    const int R = a.rows_per_warp;  // ≤ 32
+    const int tile = blockIdx.x;
+    const int strip = blockIdx.y;
+    const int d0 = strip * C_::DT;
+
+    if (threadIdx.x == 0) {
+        kr[0] = INT_MAX;
+        kr[1] = -1;
+        kr[2] = 0;
+        mbar_init(smem_addr(&bars[0]), 1);
+        mbar_init(smem_addr(&bars[1]), 1);
+        fence_barrier_init();
+        prefetch_tensor_map(&tmY);
+    }
+
+    int my_row = -1, my_start = 0, my_end = 0;
+    if (lane < R) {
+        const long long m = sched_pos(tile, sched_slot(lane, warp, W), a.tiles_per_block, a.seg_rows, a.M);
+        if (m >= 0) {
+            const int r = a.perm ? __ldg(a.perm + m) : (int)m;
+            if ((unsigned)r < (unsigned)a.M) {
+                int s = __ldg(a.row_offsets + r), e = __ldg(a.row_offsets + r + 1);
+                s = min(max(s, 0), a.nnz);
+                e = min(max(e, s), a.nnz);
+                my_row = r;
+                my_start = s;
+                my_end = e;
+            }
+        }
+    }
+    int kmin = INT_MAX, kmax = -1;
+    if (my_end > my_start) {
+        kmin = __ldg(a.col_indices + my_start);
+        kmax = __ldg(a.col_indices + my_end - 1);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(kFullMask, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(kFullMask, kmax, o));
+    }
+    __syncthreads();
+    if (lane == 0 && kmax >= 0) {
+        atomicMin(&kr[0], kmin);
+        atomicMax(&kr[1], kmax);
+    }
+    __syncthreads();
+    // The tile's chunks [c_lo, c_lo + nchunks) are split into gridDim.z
+    // contiguous ranges, one per CTA on z: every nonzero falls in exactly one.
+    int c_lo = 0, nchunks = 0;
+    {
+        const int lo = max(kr[0], 0), hi = min(kr[1], a.K - 1);
+        if (kr[1] >= 0 && lo <= hi) {
+            const int per = (hi / KC - lo / KC + 1 + gridDim.z - 1) / gridDim.z;
+            const int first = lo / KC + blockIdx.z * per;
+            c_lo = first;
+            nchunks = max(0, min(hi / KC + 1, first + per) - first);
+        }
+    }
+    // Later ranges start each row at its first nonzero in range (binary search
+    // of the sorted column indices; lanes < R, overlapping the first copy).
+    const bool later = blockIdx.z > 0 && nchunks > 0;
+
+    auto issue = [&](int j) {
+        const int s = j % NS;
+        const uint32_t bar = smem_addr(&bars[s]);
+        mbar_arrive_expect_tx(bar, STAGE);
+        const uint32_t dst = smem_addr(stages + s * STAGE);
+#pragma unroll
+        for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
+            tma_load_2d(dst + b * C_::BOX_ROWS * PITCH, &tmY, d0, (c_lo + j) * KC + b * C_::BOX_ROWS,
+                        bar);
+    };
+    if (threadIdx.x == 0) {
+        if (nchunks > 0) issue(0);
+        if (NS > 1 && nchunks > 1) issue(1);
+    }
+    if (later && my_end > my_start) {
+        const int k_first = c_lo * KC;
+        int lo = my_start, hi = my_end;  // first position with column >= k_first
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(a.col_indices + mid) < k_first) lo = mid + 1;
+            else hi = mid;
+        }
+        my_start = lo;
+    }
+
+    int cur = my_start;
+    // Prefetched state of the next row to process: its window and X strip.
+    int pcol = window_col(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), lane);
+    uint32_t pxw[XW];
+    load_x<BF, L, VV>(a, __shfl_sync(kFullMask, my_row, 0), d0, l, pxw);
+
+    uint32_t* wl = lists + warp * 32;
+    // Entry e of a window goes to slot (e % G)·L + e / G, so group g finds
+    // its steps 0..L-1 contiguous at g·L and reads four per 128-bit load.
+    const int my_slot = (lane % G) * L + lane / G;
+    const uint32_t gl = smem_addr(wl + g * L);
+    const bool single_strip = gridDim.y == 1;
+
+    for (int j = 0; j < nchunks; ++j) {
+        const int s = j % NS;
+        const int k0 = (c_lo + j) * KC;
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs);
+        if (!ok) kr[2] = 1;
+        const uint32_t stage = smem_addr(stages + s * STAGE) + l * 16;
+        if (ok) {
+#pragma unroll 1
+            for (int i = 0; i < R; ++i) {
+                int rc = __shfl_sync(kFullMask, cur, i);
+                const int re = __shfl_sync(kFullMask, my_end, i);
+                int col = pcol;
+                uint32_t xw[XW];
+#pragma unroll
+                for (int q = 0; q < XW; ++q) xw[q] = pxw[q];
+                // Prefetch the next row slot (slot 0 for the next chunk: its
+                // cursor is final once slot 0 has been processed, when R > 1;
+                // for R == 1 the reload after the segment covers it).
+                {
+                    const int ni = (i + 1 < R) ? i + 1 : 0;
+                    if (ni != i) {
+                        pcol = window_col(a, __shfl_sync(kFullMask, cur, ni),
+                                          __shfl_sync(kFullMask, my_end, ni), lane);
+                        load_x<BF, L, VV>(a, __shfl_sync(kFullMask, my_row, ni), d0, l, pxw);
+                    }
+                }
+                while (true) {
+                    const bool valid = (rc + lane < re) && ((unsigned)(col - k0) < (unsigned)KC);
+                    const unsigned bal = __ballot_sync(kFullMask, valid);
+                    const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);
+                    if (n == 0) break;
+                    // A full window may continue: fetch the next one now so its
+                    // latency overlaps this window's work.
+                    const int ncol = (n == 32) ? window_col(a, rc + 32, re, lane) : INT_MAX;
+                    wl[my_slot] = (lane < n) ? (uint32_t)(col - k0) * PITCH : 0u;
+                    __syncwarp();
+                    float part[L];
+#pragma unroll
+                    for (int t4 = 0; t4 < L; t4 += 4) {
+                        if (t4 * G < n) {
+                            const uint4 o4 = lds128(gl + t4 * 4);
+                            const uint32_t off[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                part[t4 + u] = ((t4 + u) * G < n) ? lane_dot<BF, L, VV>(xw, stage + off[u]) : 0.f;
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) part[t4 + u] = 0.f;
+                        }
+                    }
+                    // Transpose-reduce across the L lanes of each group: after it,
+                    // lane l holds the group's sum for step l.
+#pragma unroll
+                    for (int off = L / 2; off >= 1; off >>= 1) {
+                        const bool upper = (l & off) != 0;
+#pragma unroll
+                        for (int q = 0; q < off; ++q) {
+                            const float send = upper ? part[q] : part[q + off];
+                            const float keep = upper ? part[q + off] : part[q];
+                            part[q] = keep + __shfl_xor_sync(kFullMask, send, off);
+                        }
+                    }
+                    const int e = l * G + g;  // window entry whose sum this lane holds
+                    if (e < n) {
+                        const long long p = (long long)rc + e;
+                        if (single_strip) {
+                            const float v = a.scale ? part[0] * scale_at(a.scale, a.scale_bf16, p) : part[0];
+                            if (a.out_bf16)
+                                reinterpret_cast<uint16_t*>(a.out)[p] = f32_to_bf16_rne(v);
+                            else
+                                reinterpret_cast<float*>(a.out)[p] = v;
+                        } else {
+                            reinterpret_cast<float*>(a.out)[(long long)strip * a.out_stride + p] = part[0];
+                        }
+                    }
+                    __syncwarp();
+                    rc += n;
+                    if (n < 32) break;
+                    col = ncol;
+                }
+                if (lane == i) cur = rc;
+                if (R == 1) {
+                    pcol = window_col(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0),
+                                      lane);
+                }
+            }
+        }
+        __syncthreads();
+        if (kr[2]) break;
+        if (threadIdx.x == 0 && j + NS < nchunks) {
+            fence_proxy_async_smem();
+            issue(j + NS);
+        }
+    }
+
+    if (kr[2] && threadIdx.x == 0) {
+        record_status(a.status, USM_ERR_TIMEOUT);
+        for (int b = 0; b < NS && b < nchunks; ++b) {
+            mbar_wait_bounded(smem_addr(&bars[b]), 0, 1000000ull);
+            mbar_wait_bounded(smem_addr(&bars[b]), 1, 1000000ull);
+        }
+    }
+}
+
+// out[p] = Σ_s partial[s][p] (strips added in increasing order), times the
+// mask's value when scaling.
+__global__ void sddmm_strip_sum_kernel(const float* __restrict__ part, long long nnz, int nstrips,
+                                       void* out, int out_bf16, const void* scale, int scale_bf16) {
+    for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < nnz;
+         p += (long long)gridDim.x * blockDim.x) {
+        float s = part[p];
+        for (int k = 1; k < nstrips; ++k) s += part[(long long)k * nnz + p];
+        if (scale) s *= scale_at(scale, scale_bf16, p);
+        if (out_bf16)
+            reinterpret_cast<uint16_t*>(out)[p] = f32_to_bf16_rne(s);
+        else
+            reinterpret_cast<float*>(out)[p] = s;
+    }
+}
+
+// The same sum four nonzeros at a time with 16-byte loads of every strip's
+// partials (nnz a multiple of 4, partials, out and scale aligned to the
+// vector): several loads in flight per thread instead of one.
+__global__ void sddmm_strip_sum4_kernel(const float4* __restrict__ part, long long n4, int nstrips, void* out,
+                                        int out_bf16, const void* scale, int scale_bf16) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+         i += (long long)gridDim.x * blockDim.x) {
+        float4 s = __ldcs(part + i);
+#pragma unroll 4
+        for (int k = 1; k < nstrips; ++k) {
+            const float4 v = __ldcs(part + (long long)k * n4 + i);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        if (scale) {
+            if (scale_bf16) {
+                const uint2 b = __ldg(reinterpret_cast<const uint2*>(scale) + i);
+                s.x *= __uint_as_float(b.x << 16);
+                s.y *= __uint_as_float(b.x & 0xffff0000u);
+                s.z *= __uint_as_float(b.y << 16);
+                s.w *= __uint_as_float(b.y & 0xffff0000u);
+            } else {
+                const float4 c = __ldg(reinterpret_cast<const float4*>(scale) + i);
+                s.x *= c.x;
+                s.y *= c.y;
+                s.z *= c.z;
+                s.w *= c.w;
+            }
+        }
+        if (out_bf16) {
+            const uint32_t lo = (uint32_t)f32_to_bf16_rne(s.x) | ((uint32_t)f32_to_bf16_rne(s.y) << 16);
+            const uint32_t hi = (uint32_t)f32_to_bf16_rne(s.z) | ((uint32_t)f32_to_bf16_rne(s.w) << 16);
+            reinterpret_cast<uint2*>(out)[i] = make_uint2(lo, hi);
+        } else {
+            reinterpret_cast<float4*>(out)[i] = s;
+        }
+    }
+}
+
+__global__ void fill_out_kernel(void* out, long long n, int bf16) {
+    for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n;
+         p += (long long)gridDim.x * blockDim.x) {
+        if (bf16)
+            reinterpret_cast<uint16_t*>(out)[p] = 0;
+        else
+            reinterpret_cast<float*>(out)[p] = 0.f;
+    }
+}
+
+// 32×32 tiles through shared memory (padded against bank conflicts).
+template <typename T>
+__global__ void dense_transpose_kernel(const T* __restrict__ src, long long lds, int rows, int cols,
+                                       T* __restrict__ dst, long long ldd) {
+    __shared__ T tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[i][threadIdx.x] = src[(long long)r * lds + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, r = r0 + threadIdx.x;
+        if (r < rows && c < cols) dst[(long long)c * ldd + r] = tile[threadIdx.x][i];
+    }
+}
+
+}  // namespace
+}  // namespace usm

@@ -1,0 +1,474 @@
+// CSR SpMM, C = A·B, for sm_103a.
+//
+// "Sparse GPU Kernels for Deep Learning" (Gale et al., SC 2020), summary
+// card "Summary": SpMM on plain CSR with 1-D tiling, vector memory access on
+// misaligned sparse rows and a load-balancing order kept apart from how the
+// work is split ("Interesting ideas" I4).  The design below is written for
+// GB300, not taken from the V100 kernels:
+//
+// * 1-D tiles.  A CTA owns MT = R·W rows of A and one strip of NT output
+//   columns; the row scheduler (sched_pos) deals the row-swizzle order out to
+//   tiles and warps boustrophedon-fashion, so every tile and warp gets a
+//   similar mix of row lengths even when lengths are skewed.  Each output element is accumulated by
+//   exactly one lane group in a fixed order: results do not depend on the
+//   swizzle.  bf16 runs two CTAs per SM, so one CTA's barrier waits and
+//   prologue overlap the other's arithmetic; fp32, bound by shared-memory
+//   bandwidth, runs one CTA per SM with more registers and a taller stage.
+// * Dense operand staging.  The CTA walks K in chunks of KC rows.  For each
+//   chunk one thread issues TMA tensor copies of B[k0:k0+KC, n0:n0+NT] into a
+//   shared-memory stage (completion on an mbarrier, bounded wait; one or two
+//   stages).  Only the chunks between the smallest and largest column index of
+//   the CTA's rows are fetched, so block-diagonal (batched) matrices stay
+//   cheap.
+// * Sparse operand.  For each (row, chunk) a warp reads the next 32 column
+//   indices and values of the row with coalesced loads (the window after the
+//   row's cursor, so a misaligned row start costs nothing), keeps the prefix
+//   whose columns fall in the chunk (ballot) and writes (stage offset, value)
+//   entries to a per-warp list.  The next row's window is prefetched while
+//   the current one computes.
+// * Inner loop.  G = 32/L lane groups split the list into contiguous blocks.
+//   Four steps at a time a group reads its four entries with 128-bit
+//   broadcast loads (then 0-3 single steps), each lane reads 16 (fp32) or 8
+//   (bf16) bytes of the staged B row (a group covers whole rows,
+//   conflict-free) and does 4 FMAs: packed f32x2 FMA for fp32,
+//   fma.rn.f32.bf16 on the bf16 halves for bf16.  The G partial rows are
+//   added across groups at the end.
+// * Accuracy.  In fp32 each window of ≤ 32 nonzeros is summed into a fresh
+//   accumulator, windows are added into a per-(row, chunk) partial and those
+//   into the row total: with ≤ 32 + 7 + K/KC additions along any output's
+//   path the worst-case rounding bound stays below 1e-5·Σ|a||b| while
+//   K/KC ≤ 128 (K up to 12288 with KC = 96).
+#pragma once
+
+#include <climits>
+#include <type_traits>
+
+#include "usm_device.cuh"
+#include "usm_args.h"
+
+namespace usm {
+namespace {
+
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS>
+struct SpmmCfg {
+    static constexpr int ES = BF ? 2 : 4;          // element bytes
+    static constexpr int NT = L * VEC;             // output columns per CTA (VEC per lane)
+    static constexpr int G = 32 / L;               // lane groups (nonzeros per warp step)
+    static constexpr int LANE_BYTES = VEC * ES;    // B bytes per lane per step
+    static constexpr int NCH = LANE_BYTES / 16;    // 16-byte loads per lane per step (0: one 8-byte load)
+    // The stage holds NBOX TMA boxes side by side in memory, each KC rows of
+    // BOX_COLS columns (a box is at most 256 elements wide).
+    static constexpr int BOX_COLS = NT <= 256 ? NT : 256;
+    static constexpr int NBOX = NT / BOX_COLS;
+    static constexpr int PITCH = BOX_COLS * ES;    // bytes per staged row of one box
+    static constexpr int NW = LANE_BYTES / 4;      // 32-bit words per lane per step
+    static constexpr int BOX_BYTES = KC * PITCH;
+    static constexpr int STAGE = NBOX * BOX_BYTES;
+    static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
+    static constexpr int THREADS = W * 32;
+    // List entries.  fp32: (stage offset, value bits), 8 bytes.  bf16 with
+    // 8-byte lane slices (ADDR): an array of shared-memory row addresses and
+    // one of bf16 values, 6 bytes, so a step needs one add for its address.
+    // bf16 with 16-byte slices: offset/8 | value << 16 in 4 bytes (the extra
+    // value load of the split form cost more than its saved arithmetic there).
+    static constexpr bool ADDR = BF && NCH == 0;
+    static constexpr int ENTRY = ADDR ? 6 : (BF ? 4 : 8);
+    static constexpr int LIST_BYTES = W * 32 * ENTRY;
+    static constexpr int SMEM = NS * STAGE + 64 + LIST_BYTES;
+    static_assert(NS == 1 || NS == 2, "one or two stages");
+    static_assert(32 % L == 0, "L must divide the warp");
+    static_assert(KC % BOX_ROWS == 0 && BOX_ROWS <= 256, "TMA box height");
+    static_assert(LANE_BYTES == 8 || LANE_BYTES == 16 || LANE_BYTES == 32, "8, 16 or 32 bytes per lane");
+    // Byte offset, from a staged row's start in box 0, of 16-byte piece c of
+    // a lane's slice (lane offset excluded): piece c covers bytes
+    // [c·L·16, (c+1)·L·16) of the row, which may lie in a later box.
+    static constexpr int piece_off(int c) { return (c * L * 16) / PITCH * BOX_BYTES + (c * L * 16) % PITCH; }
+    static_assert(NT % BOX_COLS == 0 && (NCH == 0 || PITCH % (L * 16) == 0), "16-byte pieces tile the boxes");
+    static_assert(!BF || ADDR || BOX_BYTES / 8 < 65536, "packed bf16 offsets are 16-bit multiples of 8 bytes");
+};
+
+// Output column (within the strip) of element v of lane l.  8-byte lanes own
+// VEC contiguous columns; wider lanes own one 16-byte chunk per L·16-byte
+// slice of the staged row, so every warp-wide load reads contiguous bytes.
+template <int L, int VEC, int ES>
+__device__ __forceinline__ int lane_col(int l, int v) {
+    constexpr int EPC = 16 / ES;
+    if constexpr (VEC * ES == 8) return l * VEC + v;
+    return (v / EPC) * L * EPC + l * EPC + (v % EPC);
+}
+
+// Window of 32 consecutive nonzeros of a row starting at `pos`: lane i gets
+// nonzero pos+i (column INT_MAX past the row end).
+template <bool BF>
+__device__ __forceinline__ void load_window(const SpmmArgs& a, int pos, int end, int lane, int& col,
+                                            uint32_t& val) {
+    const int p = pos + lane;
+    if (p < end) {
+        col = __ldg(a.col_indices + p);
+        if (BF)
+            val = __ldg(reinterpret_cast<const unsigned short*>(a.values) + p);
+        else
+            val = __ldg(reinterpret_cast<const unsigned int*>(a.values) + p);
+    } else {
+        col = INT_MAX;
+        val = 0;
+    }
+}
+
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB>
+__global__ void __launch_bounds__(W * 32, MB)
+    spmm_kernel(const __grid_constant__ CUtensorMap tmB, const SpmmArgs a) {
+    using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
+    constexpr int NCH = C_::NCH, NW = C_::NW;
+    constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, ENTRY = C_::ENTRY;
+    constexpr bool ADDR = C_::ADDR;
+
+    extern __shared__ __align__(1024) unsigned char smem[];
+    unsigned char* stages = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
+    int* kr = reinterpret_cast<int*>(smem + NS * STAGE + 16);  // [0]=min col, [1]=max col, [2]=abort
+    unsigned char* lists = smem + NS * STAGE + 64;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane / L, l = lane % L;
+    const int n0 = blockIdx.y * C_::NT;
+    const int tile = blockIdx.x;
+
+    if (threadIdx.x == 0) {
+        kr[0] = INT_MAX;
+        kr[1] = -1;
+        kr[2] = 0;
+        mbar_init(smem_addr(&bars[0]), 1);
+        mbar_init(smem_addr(&bars[1]), 1);
+        fence_barrier_init();
+        prefetch_tensor_map(&tmB);
+    }
+
+    // Row slots of this warp: slot i is row perm[tile*MT + i*W + warp].
+    int my_row = -1, my_start = 0, my_end = 0;
+    if (lane < R) {
+        const long long m = sched_pos(tile, sched_slot(lane, warp, W), a.tiles_per_block, a.seg_rows, a.M);
+        if (m >= 0) {
+            const int r = a.perm ? __ldg(a.perm + m) : (int)m;
+            if ((unsigned)r < (unsigned)a.M) {
+                int s = __ldg(a.row_offsets + r), e = __ldg(a.row_offsets + r + 1);
+                s = min(max(s, 0), a.nnz);
+                e = min(max(e, s), a.nnz);
+                my_row = r;
+                my_start = s;
+                my_end = e;
+            }
+        }
+    }
+    int kmin = INT_MAX, kmax = -1;
+    if (my_end > my_start) {
+        kmin = __ldg(a.col_indices + my_start);
+        kmax = __ldg(a.col_indices + my_end - 1);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(kFullMask, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(kFullMask, kmax, o));
+    }
+    __syncthreads();
+    if (lane == 0 && kmax >= 0) {
+        atomicMin(&kr[0], kmin);
+        atomicMax(&kr[1], kmax);
+    }
+    __syncthreads();
+    int c_lo = 0, nchunks = 0;
+    {
+        const int lo = max(kr[0], 0), hi = min(kr[1], a.K - 1);
+        if (kr[1] >= 0 && lo <= hi) {
+            c_lo = lo / KC;
+            nchunks = hi / KC - c_lo + 1;
+        }
+    }
+
+    auto issue = [&](int j) {
+        const int s = j % NS;
+        const uint32_t bar = smem_addr(&bars[s]);
+        mbar_arrive_expect_tx(bar, STAGE);
+        const uint32_t dst = smem_addr(stages + s * STAGE);
+#pragma unroll
+        for (int x = 0; x < C_::NBOX; ++x)
+#pragma unroll
+            for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
+                tma_load_2d(dst + x * C_::BOX_BYTES + b * C_::BOX_ROWS * PITCH, &tmB, n0 + x * C_::BOX_COLS,
+                            (c_lo + j) * KC + b * C_::BOX_ROWS, bar);
+    };
+    if (threadIdx.x == 0) {
+        if (nchunks > 0) issue(0);
+        if (NS > 1 && nchunks > 1) issue(1);
+    }
+
+    float acc[R][VEC];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[i][v] = 0.f;
+
+    int cur = my_start;  // lane i: cursor of row slot i
+    // PERSIST (one CTA per SM, registers to spare): each row slot keeps a
+    // 32-entry window of its CSR arrays in registers across chunks (lane e
+    // holds entry wb[i] + e), so at high sparsity one window serves several
+    // chunks.  Otherwise (two CTAs per SM, 64 registers) the window of the
+    // next row slot is fetched while the current one computes.
+    constexpr bool PERSIST = MB == 1;
+    constexpr int RW = PERSIST ? R : 1;
+    int wcol[RW];
+    uint32_t wval[RW];
+    int wb[RW];
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+        wb[i] = __shfl_sync(kFullMask, cur, i);
+        load_window<BF>(a, wb[i], __shfl_sync(kFullMask, my_end, i), lane, wcol[i], wval[i]);
+    }
+
+    unsigned char* wl = lists + warp * 32 * ENTRY;
+    const uint32_t wl_addr = smem_addr(wl);
+
+    for (int j = 0; j < nchunks; ++j) {
+        const int s = j % NS;
+        const int k0 = (c_lo + j) * KC;
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs);
+        if (!ok) kr[2] = 1;
+        const uint32_t stage0 = smem_addr(stages + s * STAGE);
+        const uint32_t lane_off = l * (NCH ? 16 : 8);
+        const uint32_t stage = stage0 + lane_off;
+        if (ok) {
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                int rc = __shfl_sync(kFullMask, cur, i);
+                const int re = __shfl_sync(kFullMask, my_end, i);
+                int col = wcol[PERSIST ? i : 0];
+                uint32_t val = wval[PERSIST ? i : 0];
+                int base = PERSIST ? wb[i] : rc;  // position of the window's lane 0 (rc - base < 32)
+                if constexpr (!PERSIST) {
+                    if (i + 1 < R) {
+                        wb[0] = __shfl_sync(kFullMask, cur, i + 1);
+                        load_window<BF>(a, wb[0], __shfl_sync(kFullMask, my_end, i + 1), lane, wcol[0], wval[0]);
+                    }
+                }
+                float c4[BF ? 1 : VEC];  // fp32: this window's partial sums (≤ 32 terms)
+                float cc[BF ? 1 : VEC];  // fp32: this chunk segment's windows
+#pragma unroll
+                for (int v = 0; v < (BF ? 1 : VEC); ++v) c4[v] = cc[v] = 0.f;
+                while (true) {
+                    // The chunk's entries of this row: a run of the window from
+                    // lane rc - base (columns are sorted).
+                    const int wo = PERSIST ? rc - base : 0;  // without PERSIST the window starts at rc
+                    const bool valid = lane >= wo && (base + lane < re) && ((unsigned)(col - k0) < (unsigned)KC);
+                    const unsigned run = __ballot_sync(kFullMask, valid) >> wo;
+                    const int n = (run == kFullMask) ? 32 : (__ffs(~run) - 1);
+                    if (n == 0) break;
+                    // The window runs out inside this chunk: fetch the next one
+                    // now so its latency overlaps this window's work.
+                    const bool more = wo + n == 32;
+                    int ncol = INT_MAX;
+                    uint32_t nval = 0;
+                    if (more) load_window<BF>(a, base + 32, re, lane, ncol, nval);
+                    // G == 1: exact count (0-3 single steps at the end).  G > 1: each
+                    // group's block must start 16-byte aligned for the 128-bit
+                    // entry loads, so pad to a multiple of 4·G.  Lane e writes
+                    // list slot (e - wo) mod 32: every slot below npad is written.
+                    const int npad = (G == 1) ? n : (n + 4 * G - 1) / (4 * G) * (4 * G);
+                    const int slot = (lane - wo) & 31;
+                    if (slot < npad) {
+                        const bool live = slot < n;
+                        const uint32_t off = live ? (uint32_t)(col - k0) * PITCH : 0u;
+                        if constexpr (ADDR) {
+                            reinterpret_cast<uint32_t*>(wl)[slot] = stage0 + off;
+                            reinterpret_cast<uint16_t*>(wl + 128)[slot] = live ? (uint16_t)val : (uint16_t)0;
+                        } else if constexpr (BF) {
+                            reinterpret_cast<uint32_t*>(wl)[slot] = live ? ((off >> 3) | (val << 16)) : 0u;
+                        } else {
+                            reinterpret_cast<uint2*>(wl)[slot] = live ? make_uint2(off, val) : make_uint2(0u, 0u);
+                        }
+                    }
+                    __syncwarp();
+                    const int q = npad / G;  // steps of each group
+                    const int q4 = q & ~3;
+                    const uint32_t gl = wl_addr + g * q * (ADDR ? 4 : ENTRY);  // ADDR: addresses
+                    const uint32_t gv = wl_addr + 128 + g * q * 2;             // ADDR: values
+                    // The lane's words of the staged B row whose lane slice starts at p.
+                    auto load_b = [&](uint32_t p, uint32_t (&w)[NW]) {
+                        if constexpr (NCH == 0) {
+                            const uint2 b = lds64(p);
+                            w[0] = b.x;
+                            w[1] = b.y;
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < NCH; ++c) {
+                                const uint4 b = lds128(p + C_::piece_off(c));
+                                w[4 * c] = b.x;
+                                w[4 * c + 1] = b.y;
+                                w[4 * c + 2] = b.z;
+                                w[4 * c + 3] = b.w;
+                            }
+                        }
+                    };
+                    // One bf16 step: staged row at shared address ad, value av.
+                    auto step_bf16 = [&](uint32_t ad, uint16_t av) {
+                        uint32_t w[NW];
+                        load_b(ad + lane_off, w);
+#pragma unroll
+                        for (int q = 0; q < NW; ++q) {
+                            acc[i][2 * q] = fma_bf16(av, lo16(w[q]), acc[i][2 * q]);
+                            acc[i][2 * q + 1] = fma_bf16(av, hi16(w[q]), acc[i][2 * q + 1]);
+                        }
+                    };
+                    // One fp32 step: staged row at byte offset off, value bits av.
+                    auto step_f32 = [&](uint32_t off, uint32_t av) {
+                        uint32_t w[NW];
+                        load_b(stage + off, w);
+                        const float x = __uint_as_float(av);
+                        const float2 a2 = make_float2(x, x);
+#pragma unroll
+                        for (int q = 0; q < NW; q += 2) {
+                            float2 c2 = make_float2(c4[q], c4[q + 1]);
+                            c2 = __ffma2_rn(a2, make_float2(__uint_as_float(w[q]), __uint_as_float(w[q + 1])), c2);
+                            c4[q] = c2.x;
+                            c4[q + 1] = c2.y;
+                        }
+                    };
+#pragma unroll 1
+#pragma unroll 1
+                    for (int t = 0; t < q4; t += 4) {
+                        if constexpr (ADDR) {
+                            const uint4 ad = lds128(gl + t * 4);
+                            const uint2 av = lds64(gv + t * 2);
+                            step_bf16(ad.x, lo16(av.x));
+                            step_bf16(ad.y, hi16(av.x));
+                            step_bf16(ad.z, lo16(av.y));
+                            step_bf16(ad.w, hi16(av.y));
+                        } else if constexpr (BF) {
+                            const uint4 e = lds128(gl + t * 4);
+                            step_bf16(stage0 + ((e.x & 0xffffu) << 3), hi16(e.x));
+                            step_bf16(stage0 + ((e.y & 0xffffu) << 3), hi16(e.y));
+                            step_bf16(stage0 + ((e.z & 0xffffu) << 3), hi16(e.z));
+                            step_bf16(stage0 + ((e.w & 0xffffu) << 3), hi16(e.w));
+                        } else {
+                            const uint4 e01 = lds128(gl + t * 8);
+                            const uint4 e23 = lds128(gl + t * 8 + 16);
+                            step_f32(e01.x, e01.y);
+                            step_f32(e01.z, e01.w);
+                            step_f32(e23.x, e23.y);
+                            step_f32(e23.z, e23.w);
+                        }
+                    }
+#pragma unroll 1
+                    for (int t = q4; t < q; ++t) {  // 0-3 remaining steps (G == 1 only)
+                        if constexpr (ADDR) {
+                            step_bf16(lds32(gl + t * 4), lds16(gv + t * 2));
+                        } else if constexpr (BF) {
+                            const uint32_t e = lds32(gl + t * 4);
+                            step_bf16(stage0 + ((e & 0xffffu) << 3), hi16(e));
+                        } else {
+                            const uint2 e = lds64(gl + t * 8);
+                            step_f32(e.x, e.y);
+                        }
+                    }
+                    __syncwarp();
+                    if constexpr (!BF) {
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) {
+                            cc[v] += c4[v];
+                            c4[v] = 0.f;
+                        }
+                    }
+                    rc += n;
+                    if (!more) break;
+                    col = ncol;
+                    val = nval;
+                    base += 32;
+                }
+                if constexpr (!BF) {
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) acc[i][v] += cc[v];
+                }
+                if constexpr (PERSIST) {
+                    // Half the window used: refill it from the cursor now; the
+                    // load lands while the other rows and the next chunk's wait
+                    // go by.
+                    if (rc - base >= 16 && rc < re) {
+                        base = rc;
+                        load_window<BF>(a, rc, re, lane, col, val);
+                    }
+                    wcol[i] = col;
+                    wval[i] = val;
+                    wb[i] = base;
+                }
+                if (lane == i) cur = rc;
+                if constexpr (!PERSIST) {
+                    if (i + 1 == R)
+                        load_window<BF>(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), lane,
+                                        wcol[0], wval[0]);
+                }
+            }
+        }
+        __syncthreads();  // every warp is done with stage s
+        if (kr[2]) break;
+        if (threadIdx.x == 0 && j + NS < nchunks) {
+            fence_proxy_async_smem();
+            issue(j + NS);
+        }
+    }
+
+    if (kr[2]) {
+        // A transfer never completed: record it, wait (bounded) for the copies
+        // still in flight so none lands after the CTA exits, and leave.
+        if (threadIdx.x == 0) {
+            record_status(a.status, USM_ERR_TIMEOUT);
+            for (int b = 0; b < nchunks && b < NS; ++b) {
+                // Waiting on both parities waits for the barrier's current phase
+                // (the other parity reports complete at once); each wait is bounded.
+                mbar_wait_bounded(smem_addr(&bars[b]), 0, 1000000ull);
+                mbar_wait_bounded(smem_addr(&bars[b]), 1, 1000000ull);
+            }
+        }
+        return;
+    }
+
+    // Add the G partial rows held by the lane groups.
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            float x = acc[i][v];
+            if (G >= 2) x += __shfl_xor_sync(kFullMask, x, L);
+            if (G >= 4) x += __shfl_xor_sync(kFullMask, x, 2 * L);
+            if (G >= 8) x += __shfl_xor_sync(kFullMask, x, 4 * L);
+            acc[i][v] = x;
+        }
+
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int row = __shfl_sync(kFullMask, my_row, i);
+        if (row < 0 || g != 0) continue;
+        float* crow = a.C + (long long)row * a.ldc + n0;
+#pragma unroll
+        for (int v = 0; v < VEC; v += 4) {  // 4 contiguous columns at a time
+            const int c = lane_col<L, VEC, C_::ES>(l, v);
+            if (n0 + c + 4 <= a.N) {
+                *reinterpret_cast<float4*>(crow + c) = make_float4(acc[i][v], acc[i][v + 1], acc[i][v + 2], acc[i][v + 3]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (n0 + c + u < a.N) crow[c + u] = acc[i][v + u];
+            }
+        }
+    }
+}
+
+__global__ void fill_f32_kernel(float* C, int M, int N, long long ldc) {
+    const long long total = (long long)M * N;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / N, c = i % N;
+        C[r * ldc + c] = 0.f;
+    }
+}
+
+}  // namespace
+}  // namespace usm
