@@ -467,11 +467,17 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(op):
+    """Hash of the device code (comments and whitespace removed, so only a
+    change to the code itself retires a recorded capture)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES["spmm" if op.startswith("spmm") else "sddmm"]:
-        with open(os.path.join(ROOT, "unstructured_sparse_matmul_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "unstructured_sparse_matmul_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

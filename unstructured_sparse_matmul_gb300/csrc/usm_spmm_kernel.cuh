@@ -6,12 +6,13 @@
 // work is split ("Interesting ideas" I4).  The design below is written for
 // GB300, not taken from the V100 kernels:
 //
-// * 1-D tiles.  A CTA owns MT = R·W rows of A and one strip of NT output
-//   columns; the row scheduler (sched_pos) deals the row-swizzle order out to
-//   tiles and warps boustrophedon-fashion, so every tile and warp gets a
-//   similar mix of row lengths even when lengths are skewed.  Each output element is accumulated by
-//   exactly one lane group in a fixed order: results do not depend on the
-//   swizzle.  bf16 runs two CTAs per SM, so one CTA's barrier waits and
+// * 1-D tiles.  A CTA owns one row tile (at most R·W rows of A) and one
+//   strip of NT output columns; the row scheduler (sched_pos) deals the
+//   row-swizzle order out to tiles and warps boustrophedon-fashion, so every
+//   tile and warp gets a similar mix of row lengths even when lengths are
+//   skewed (the launch code picks R and the tiles per block).  Each output
+//   element is accumulated by exactly one lane group in a fixed order:
+//   results do not depend on the swizzle or the tile shape.  bf16 runs two CTAs per SM, so one CTA's barrier waits and
 //   prologue overlap the other's arithmetic; fp32, bound by shared-memory
 //   bandwidth, runs one CTA per SM with more registers and a taller stage.
 // * Dense operand staging.  The CTA walks K in chunks of KC rows.  For each
@@ -24,15 +25,18 @@
 //   indices and values of the row with coalesced loads (the window after the
 //   row's cursor, so a misaligned row start costs nothing), keeps the prefix
 //   whose columns fall in the chunk (ballot) and writes (stage offset, value)
-//   entries to a per-warp list.  The next row's window is prefetched while
-//   the current one computes.
+//   entries to a per-warp list.  With one CTA per SM each row slot keeps its
+//   window in registers across chunks (refilled from the cursor once half
+//   used); with two, the next row slot's window is fetched while the current
+//   one computes.
 // * Inner loop.  G = 32/L lane groups split the list into contiguous blocks.
 //   Four steps at a time a group reads its four entries with 128-bit
-//   broadcast loads (then 0-3 single steps), each lane reads 16 (fp32) or 8
-//   (bf16) bytes of the staged B row (a group covers whole rows,
-//   conflict-free) and does 4 FMAs: packed f32x2 FMA for fp32,
-//   fma.rn.f32.bf16 on the bf16 halves for bf16.  The G partial rows are
-//   added across groups at the end.
+//   broadcast loads (then 0-3 single steps), each lane reads 8, 16 or 32
+//   bytes of the staged B row (a group covers whole rows, conflict-free) and
+//   does VEC FMAs: packed f32x2 FMA for fp32, fma.rn.f32.bf16 on the bf16
+//   halves for bf16 (one instruction an element: splitting the pairs to fp32
+//   for packed FMAs measured 10-25% slower).  The G partial rows are added
+//   across groups at the end.
 // * Accuracy.  In fp32 each window of ≤ 32 nonzeros is summed into a fresh
 //   accumulator, windows are added into a per-(row, chunk) partial and those
 //   into the row total: with ≤ 32 + 7 + K/KC additions along any output's
