@@ -96,9 +96,6 @@ __device__ __forceinline__ void record_status(int* status, int code) {
 
 // ------------------------------------------------------------- bf16 bits
 // bf16 is the top half of an fp32 bit pattern: widening is exact.
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float x) {
     // Round to nearest, ties to even, on the bit pattern (inputs finite).
     uint32_t u = __float_as_uint(x);
@@ -164,8 +161,5 @@ __device__ __forceinline__ long long sched_pos(int tile, int slot, int T, int se
 __device__ __forceinline__ int sched_slot(int i, int warp, int W) {
     return i * W + ((i & 1) ? (W - 1 - warp) : warp);
 }
-
-// Read-only streaming loads of CSR arrays.
-__device__ __forceinline__ int ldg_i32(const int* p) { return __ldg(p); }
 
 }  // namespace usm
