@@ -22,21 +22,29 @@
 #include <omp.h>
 #endif
 
+/* Threads for the next parallel loop: nthreads > 0 asks for that many, 0 for
+ * the process default (OMP_NUM_THREADS or all cores), captured on first use so
+ * an earlier call with a fixed count does not shrink later "all cores" calls. */
+static int g_default_threads = 0;
+
+static int default_threads(void) {
+#ifdef _OPENMP
+    if (g_default_threads == 0) g_default_threads = omp_get_max_threads();
+    return g_default_threads;
+#else
+    return 1;
+#endif
+}
+
 static void set_threads(int nthreads) {
 #ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
+    omp_set_num_threads(nthreads > 0 ? nthreads : default_threads());
 #else
     (void)nthreads;
 #endif
 }
 
-int oracle_max_threads(void) {
-#ifdef _OPENMP
-    return omp_get_max_threads();
-#else
-    return 1;
-#endif
-}
+int oracle_max_threads(void) { return default_threads(); }
 
 /*
  * Plain CSR contract ("Interesting ideas" I5: standard CSR, no structural

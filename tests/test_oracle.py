@@ -301,3 +301,15 @@ def test_workload_generators_produce_valid_csr():
     for p in [W.tiny(), W.resnet(with_sddmm=False)]:
         c = p.csr
         assert oracle.csr_check(c.M, c.K, c.row_offsets, c.col_indices) == 0
+
+
+def test_thread_count_is_per_call():
+    """A call pinned to one thread does not shrink later all-cores calls,
+    and every thread count gives the same bits (fixed per-row order)."""
+    csr = W.random_csr([64, 48, 7], 64, 48, 0.2)
+    B = np.random.default_rng(7).standard_normal((48, 16))
+    default = oracle.max_threads()
+    one = oracle.spmm(64, 48, csr.row_offsets, csr.col_indices, csr.values.astype(np.float64), B, 1)
+    assert oracle.max_threads() == default
+    allc = oracle.spmm(64, 48, csr.row_offsets, csr.col_indices, csr.values.astype(np.float64), B, 0)
+    assert np.array_equal(one, allc)
