@@ -458,16 +458,17 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
-# Device source files each timed operation's kernels are built from (the
-# launch code lives apart, so launch-choice changes keep a capture valid).
+# Source files that fix each timed operation's kernels and launch shapes (the
+# grid decides how often staged tiles are re-read, so a launch-model change
+# retires a capture as surely as a kernel change).
 KERNEL_SOURCES = {
-    "spmm": ("usm_spmm_kernel.cuh", "usm_device.cuh", "usm_args.h"),
-    "sddmm": ("usm_sddmm_kernel.cuh", "usm_device.cuh", "usm_args.h"),
+    "spmm": ("usm_spmm_kernel.cuh", "usm_spmm.cu", "usm_device.cuh", "usm_args.h", "usm_internal.h"),
+    "sddmm": ("usm_sddmm_kernel.cuh", "usm_sddmm.cu", "usm_device.cuh", "usm_args.h", "usm_internal.h"),
 }
 
 
 def kernel_source_hash(op):
-    """Hash of the device code (comments and whitespace removed, so only a
+    """Hash of those sources (comments and whitespace removed, so only a
     change to the code itself retires a recorded capture)."""
     import hashlib
     import re

@@ -64,10 +64,6 @@ int launch_csr_transpose(int M, int K, int nnz, const int* row_offsets, const in
 int launch_permute_values(int nnz, const int* perm, const void* values, bool bf16, void* out,
                           cudaStream_t stream);
 
-// Row tiles of MT rows when tiles may not span blocks of seg rows.
-inline long long schedule_tiles(int M, int seg, int MT) {
-    return (long long)((M + seg - 1) / seg) * ((seg + MT - 1) / MT);
-}
 inline long long block_count(int M, int seg) { return (M + seg - 1) / seg; }
 inline int effective_seg(int M, int seg_rows) { return (seg_rows <= 0 || seg_rows > M) ? M : seg_rows; }
 

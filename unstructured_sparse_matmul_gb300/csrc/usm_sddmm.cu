@@ -37,44 +37,65 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
         a.out = ws;
         a.out_stride = a.nnz;
     }
-    // Rows per warp R and K splits S from a launch time model fitted to a
-    // sweep of the FFN launches (R ∈ {1..32} × S ∈ {1..16}, fp32 and bf16,
-    // L2 flushed between calls; the choices average 3% above the best pair
-    // per launch, against 7% for R alone).  Time = (CTAs / resident slots, at
-    // least 1, plus one CTA for the tail) × per-CTA work, in units of one
-    // consumed row: staging the CTA's share of the K span (0.6 a row), its
-    // share of R·W mean-length rows, a fixed start-up (3500: first copy,
-    // cursor search, epilogue) and a latency per (row, chunk) that a warp's
-    // R rows pay one after another (220).  Splitting K costs no reduction
-    // (each nonzero belongs to one split); only split counts that give every
-    // split a different chunk range are tried.
     const int sms = sm_count_current_device();
-    const double slots = (double)sms * MINB;
+    const long long slots = (long long)sms * MINB;
+    const int seg = a.seg_rows;  // rows per diagonal block (M without blocks)
+    const long long nblk = block_count(a.M, seg);
     // A block-diagonal schedule (seg_rows < M) is taken to have square blocks.
-    const double kspan = (a.seg_rows > 0 && a.seg_rows < a.M) ? (double)min(a.K, a.seg_rows) : (double)a.K;
+    const double kspan = (seg > 0 && seg < a.M) ? (double)min(a.K, seg) : (double)a.K;
     const double mean_len = (double)a.nnz / (a.M > 0 ? a.M : 1);
     const int nch = max(1, (int)((kspan + KC - 1) / KC));
-    int R = 1, S = 1;
-    double best = 0.0;
-    for (int sp = 1; sp <= min(USM_SDDMM_MAX_SPLIT, nch); ++sp) {
-        const int per = (nch + sp - 1) / sp;
-        if ((nch + per - 1) / per != sp) continue;  // same ranges as a smaller count
-        for (int r = 1; r <= 32; r <<= 1) {
-            const double n = (double)schedule_tiles(a.M, a.seg_rows, r * W) * nstrips * sp;
-            const double work = (0.6 * kspan + (double)r * W * mean_len) * per / nch + 3500.0 + 220.0 * per * r;
-            const double c = (fmax(n / slots, 1.0) + 1.0) * work;
-            if (best == 0.0 || c < best) {
-                best = c;
-                R = r;
-                S = sp;
+    // Rows per warp R, K splits S and tiles per block T from a launch time
+    // model fitted to a sweep of the FFN launches (R ∈ {4..32}, every
+    // effective S, T the fewest tiles or the most that still fit in the same
+    // number of CTA waves; L2 flushed between calls; the model's choices sum
+    // to 1.2% above the best per launch).  Time = waves × per-CTA work, with
+    // waves = ceil(CTAs / resident slots): CTAs of a launch have near-equal
+    // work (swizzled rows), so a part-filled last wave costs a whole one and
+    // more, shorter tiles that fill it are free.  Work is counted in units of
+    // one consumed row: staging the CTA's share of the K span (0.45 a row),
+    // its share of the tile's rows, a fixed start-up (6000: first copy,
+    // cursor search, epilogue) and a latency per (row, chunk) that a warp's
+    // rows pay one after another (880).  Splitting K costs no reduction
+    // (each nonzero belongs to one split); only split counts that give every
+    // split a different chunk range are tried.
+    int R = 1, S = 1, T = 1;
+    {
+        double best = 0.0;
+        const long long tmax = max(1, (seg + W - 1) / W);  // at least one row a warp
+        for (int sp = 1; sp <= min(USM_SDDMM_MAX_SPLIT, nch); ++sp) {
+            const int per = (nch + sp - 1) / sp;
+            if ((nch + per - 1) / per != sp) continue;  // same ranges as a smaller count
+            const long long ctas_per_t = nblk * nstrips * sp;
+            for (int r = 1; r <= 32; r <<= 1) {
+                const long long t0 = (seg + r * W - 1) / (r * W);
+                const long long waves0 = (ctas_per_t * t0 + slots - 1) / slots;
+                const long long t1 = min(max(tmax, t0), max(t0, waves0 * slots / ctas_per_t));
+                for (const long long t : {t0, t1}) {
+                    const long long rows = (seg + t - 1) / t;
+                    const long long reff = (rows + W - 1) / W;
+                    const double waves = (double)((ctas_per_t * t + slots - 1) / slots);
+                    const double work =
+                        (0.45 * kspan + (double)rows * mean_len) * per / nch + 6000.0 + 880.0 * per * reff;
+                    const double c = waves * work;
+                    if (best == 0.0 || c < best) {
+                        best = c;
+                        R = (int)reff;
+                        S = sp;
+                        T = (int)t;
+                    }
+                }
             }
         }
     }
     const ScheduleOverride ov = schedule_override();
-    if (ov.rows_per_warp > 0) R = ov.rows_per_warp;
+    if (ov.rows_per_warp > 0 || ov.tiles_per_block > 0) {
+        if (ov.rows_per_warp > 0) R = ov.rows_per_warp;
+        T = max((seg + R * W - 1) / (R * W), ov.tiles_per_block);
+    }
     if (ov.k_splits > 0) S = ov.k_splits;
     a.rows_per_warp = R;
-    a.tiles_per_block = max((a.seg_rows + R * W - 1) / (R * W), ov.tiles_per_block);
+    a.tiles_per_block = T;
     const long long tiles = block_count(a.M, a.seg_rows) * a.tiles_per_block;
     if (tiles > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)tiles, nstrips, S);
