@@ -94,6 +94,8 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
         T = max((seg + R * W - 1) / (R * W), ov.tiles_per_block);
     }
     if (ov.k_splits > 0) S = ov.k_splits;
+    // Every row of a block must have a slot: tiles × R·W ≥ rows per block.
+    if (R < 1 || R > 32 || T < 1 || (long long)T * R * W < seg) return USM_ERR_INVALID_ARG;
     a.rows_per_warp = R;
     a.tiles_per_block = T;
     const long long tiles = block_count(a.M, a.seg_rows) * a.tiles_per_block;
