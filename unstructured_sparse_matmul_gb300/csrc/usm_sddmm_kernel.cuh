@@ -6,9 +6,10 @@
 // the product is X·Yᵀ), the form weight gradients and sparse-attention
 // scores need.  GB300 design:
 //
-// * Tiles.  A CTA owns MT = R·W mask rows (dealt from the row-swizzle order
-//   by the row scheduler, sched_pos; R chosen at launch) and one strip of DT
-//   columns of D.  It walks K in chunks of KC
+// * Tiles.  A CTA owns up to R·W mask rows (dealt from the row-swizzle
+//   order by the row scheduler, sched_pos; R, the tiles per block and the K
+//   splits chosen at launch), one strip of DT columns of D and one range of
+//   K chunks (grid z).  It walks its range in chunks of KC
 //   rows; one thread copies Y[k0:k0+KC, d0:d0+DT] into a shared-memory stage
 //   with TMA (mbarrier, bounded wait) into one tall stage: the tall chunks
 //   halve the per-(row, chunk) work of a double-buffered layout.  bf16 runs
