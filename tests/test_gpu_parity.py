@@ -394,7 +394,12 @@ def schedule(usm):
     usm.set_schedule_override(0, 0, 0)
 
 
-SDDMM_SCHEDULES = [(0, 0, 0), (1, 0, 1), (2, 0, 5), (8, 0, 3), (32, 0, 1), (4, 40, 2), (16, 0, 11), (1, 0, 16)]
+# (rows per warp, tiles per block, K splits); 0 keeps the library's choice.
+# Tile counts above the fewest that hold a block give tiles of fewer rows
+# (the launch model's wave-filling choice); (0, t, s) forces tiles and splits
+# under the model's own rows per warp.
+SDDMM_SCHEDULES = [(0, 0, 0), (1, 0, 1), (2, 0, 5), (8, 0, 3), (32, 0, 1), (4, 40, 2), (16, 0, 11), (1, 0, 16),
+                   (2, 44, 1), (16, 3, 0), (0, 25, 0), (0, 11, 3)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -420,7 +425,7 @@ def test_sddmm_schedules_do_not_change_bits(usm, schedule, dtype, seg):
     assert_within(outs[0], ref, S, TOL[dtype], "sddmm under forced schedules")
 
 
-SPMM_SCHEDULES = [(0, 0, 0), (2, 0, 0), (4, 0, 0), (2, 50, 0), (4, 7, 0), (0, 44, 1)]
+SPMM_SCHEDULES = [(0, 0, 0), (2, 0, 0), (4, 0, 0), (2, 50, 0), (4, 7, 0), (0, 44, 1), (0, 9, 0), (0, 30, 0)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
