@@ -15,8 +15,9 @@
  *   ("workspace"); its size comes from the matching *_workspace_bytes call.
  * CSR.  row_offsets is int32[M+1] with row_offsets[0] = 0, non-decreasing,
  *   row_offsets[M] = nnz; col_indices is int32[nnz], each row's indices
- *   strictly increasing and in [0, K).  The library does not scan the CSR
- *   (that would cost a pass over it); a CSR that breaks this contract gives
+ *   strictly increasing and in [0, K).  The compute calls do not scan the
+ *   CSR (that would cost a pass over it; csr_validate does, on request); a
+ *   CSR that breaks this contract gives
  *   undefined results but never an out-of-bounds dense access, because every
  *   column index is clamped into [0, K) before it addresses a dense operand.
  * Dense operands.  Row-major with a leading dimension (elements per row).
@@ -260,6 +261,39 @@ int usm_poll_status(void *stream);
 
 /* Human-readable name of a usm_status value (static string, never NULL). */
 const char *usm_status_string(int status);
+
+/*
+ * csr_validate — checks the CSR contract above on the device, for callers
+ * whose matrices come from outside (the pages give plain CSR, "Interesting
+ * ideas" I5; the strictly increasing column order is this library's
+ * reading).  The compute entry points never scan the CSR themselves.
+ *   result : device int[USM_CSR_VALIDATE_INTS], caller-owned, 4-byte aligned;
+ *            on completion (stream order) result[0] is a usm_csr_check code
+ *            and result[1] the first offending index (the row for offset
+ *            codes, M for USM_CSR_LAST_OFFSET, the nonzero position for
+ *            column codes; -1 when valid).  Words 2.. are scratch.
+ * Violations are reported in this order, the first that applies:
+ * row_offsets[0] != 0; offsets decreasing (first such row r:
+ * row_offsets[r+1] < row_offsets[r]); row_offsets[M] != nnz; then the first
+ * nonzero position p whose column is outside [0, K) (range) or not above the
+ * previous column of its row (order), range winning a tie.  Reads stay
+ * inside row_offsets[0..M] and col_indices[0..nnz) whatever the contents.
+ * Returns USM_ERR_INVALID_ARG for negative sizes or NULL pointers (col_indices
+ * may be NULL when nnz = 0), else USM_OK / USM_ERR_CUDA for the launch.
+ */
+typedef enum usm_csr_check {
+    USM_CSR_VALID = 0,
+    USM_CSR_FIRST_OFFSET = 1,     /* row_offsets[0] != 0 */
+    USM_CSR_OFFSETS_DECREASE = 2, /* row_offsets[r+1] < row_offsets[r] */
+    USM_CSR_LAST_OFFSET = 3,      /* row_offsets[M] != nnz */
+    USM_CSR_COLUMN_RANGE = 4,     /* col_indices[p] outside [0, K) */
+    USM_CSR_COLUMN_ORDER = 5      /* col_indices[p] <= col_indices[p-1] within a row */
+} usm_csr_check;
+
+#define USM_CSR_VALIDATE_INTS 8
+
+int csr_validate(int M, int K, int nnz, const int *row_offsets, const int *col_indices, int *result,
+                 void *stream);
 
 /*
  * usm_selftest_wait_timeout — checks the bounded-wait path without faulting

@@ -114,11 +114,16 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # Operations
 # ---------------------------------------------------------------------------
-def csr_check(M: int, K: int, row_offsets, col_indices) -> int:
+def csr_check(M: int, K: int, row_offsets, col_indices, nnz: int | None = None) -> int:
+    """0 for a valid CSR, else the negative code of the first violation
+    (usm_oracle.c).  nnz defaults to the length of col_indices."""
     ro, ci = _i32(row_offsets), _i32(col_indices)
     if ro.size != M + 1:
         return -7
-    return int(_L().oracle_csr_check(M, K, int(ro[-1]) if M >= 0 else 0, _p(ro, _i32p), _p(ci, _i32p)))
+    nnz = ci.size if nnz is None else nnz
+    if nnz > ci.size:
+        return -7
+    return int(_L().oracle_csr_check(M, K, nnz, _p(ro, _i32p), _p(ci, _i32p)))
 
 
 def spmm(M: int, K: int, row_offsets, col_indices, values64, B64, nthreads: int = 0) -> np.ndarray:

@@ -175,3 +175,14 @@ def test_schedule_override_validation(lib):
             assert f(*good) == 0, good
     finally:
         assert f(0, 0, 0) == 0
+
+
+def test_validate_rejects_bad_args_on_host(lib):
+    v = lib.csr_validate
+    assert v(-1, 4, 0, A16, A16, A16, None) == -1
+    assert v(4, -1, 0, A16, A16, A16, None) == -1
+    assert v(4, 4, -1, A16, A16, A16, None) == -1
+    assert v(4, 4, 5, A16, None, A16, None) == -1       # nonzeros need col_indices
+    assert v(4, 4, 5, None, A16, A16, None) == -1       # row_offsets always read
+    assert v(4, 4, 5, A16, A16, None, None) == -1       # nowhere to write the result
+    assert v(4, 4, 5, A16, A16, A16 + 2, None) == -2    # result not int-aligned

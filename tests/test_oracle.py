@@ -295,6 +295,15 @@ def test_csr_check_rejects_corruption():
     assert oracle.csr_check(3, 4, [0, 2, 2, 5], [0, 4, 1, 2, 3]) == -5  # col out of range
     assert oracle.csr_check(3, 4, [0, 2, 2, 5], [0, 3, 2, 2, 3]) == -6  # duplicate col
     assert oracle.csr_check(3, 4, [0, 2, 2, 5], [3, 0, 1, 2, 3]) == -6  # unsorted
+    assert oracle.csr_check(3, 4, [0, 2, 2, 4], g["ci"]) == -4          # row_offsets[M] != nnz = 5
+    assert oracle.csr_check(3, 4, [0, 2, 2, 6], g["ci"]) == -4          # past the arrays: not scanned
+    assert oracle.csr_check(3, 4, [1, 0, 2, 4], g["ci"]) == -2          # first rule wins
+    assert oracle.csr_check(3, 4, [0, 2, 1, 4], g["ci"]) == -3          # decrease before the last offset
+    # entries: the first bad nonzero decides; at one position the range test first
+    assert oracle.csr_check(3, 4, [0, 2, 2, 5], [1, 0, 1, 2, 9]) == -6  # order at p=1 before range at p=4
+    assert oracle.csr_check(3, 4, [0, 2, 2, 5], [0, 3, 1, 9, 3]) == -5  # range at p=3 before order at p=4
+    assert oracle.csr_check(3, 4, [0, 2, 2, 5], [2, -1, 1, 2, 3]) == -5  # p=1 fails both: range
+    assert oracle.csr_check(0, 4, [0], []) == 0 and oracle.csr_check(0, 4, [0], [5]) == -4
 
 
 def test_workload_generators_produce_valid_csr():

@@ -45,7 +45,13 @@ SIGNATURES = {
     "csr_row_softmax": (_i, [_i, _i, _vp, _vp, _vp, _i, _vp]),
     "csr_transpose": (_i, [_i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "csr_permute_values": (_i, [_i, _vp, _vp, _i, _vp, _vp]),
+    "csr_validate": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp]),
 }
+
+# csr_validate result codes (usm_csr_check in include/usm.h).
+CSR_CHECK = {0: "USM_CSR_VALID", 1: "USM_CSR_FIRST_OFFSET", 2: "USM_CSR_OFFSETS_DECREASE",
+             3: "USM_CSR_LAST_OFFSET", 4: "USM_CSR_COLUMN_RANGE", 5: "USM_CSR_COLUMN_ORDER"}
+CSR_VALIDATE_INTS = 8
 
 _lib = None
 _lock = threading.Lock()
@@ -275,6 +281,22 @@ def row_softmax(row_offsets, scores, out=None, out_dtype=None, stream=None):
                                _dtype_code(out), _stream(stream))
     _check("csr_row_softmax", code)
     return out
+
+
+def csr_validate(row_offsets, col_indices, K: int, stream=None):
+    """Check the CSR contract on the device: (code, index), code one of
+    CSR_CHECK (0 = valid), index the first offending row or nonzero (-1 when
+    valid).  Reads the two result words back, so it waits for the stream."""
+    torch = _torch()
+    lib = load()
+    _require(row_offsets, "row_offsets", (torch.int32,))
+    _require(col_indices, "col_indices", (torch.int32,))
+    result = torch.empty(CSR_VALIDATE_INTS, dtype=torch.int32, device=row_offsets.device)
+    code = lib.csr_validate(row_offsets.numel() - 1, K, col_indices.numel(), _ptr(row_offsets), _ptr(col_indices),
+                            _ptr(result), _stream(stream))
+    _check("csr_validate", code)
+    out = result[:2].cpu()
+    return int(out[0]), int(out[1])
 
 
 def csr_transpose(row_offsets, col_indices, values, K: int, with_perm: bool = False, stream=None):

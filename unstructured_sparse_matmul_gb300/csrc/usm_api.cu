@@ -276,6 +276,13 @@ int csr_permute_values(int nnz, const int* perm, const void* values, usm_dtype d
     return launch_permute_values(nnz, perm, values, dtype == USM_BF16, out, as_stream(stream));
 }
 
+int csr_validate(int M, int K, int nnz, const int* row_offsets, const int* col_indices, int* result, void* stream) {
+    if (M < 0 || K < 0 || nnz < 0) return USM_ERR_INVALID_ARG;
+    if (!row_offsets || !result || (nnz > 0 && !col_indices)) return USM_ERR_INVALID_ARG;
+    if ((uintptr_t)result % alignof(int) != 0) return USM_ERR_ALIGNMENT;
+    return launch_csr_validate(M, K, nnz, row_offsets, col_indices, result, as_stream(stream));
+}
+
 int usm_poll_status(void* stream) {
     cudaStream_t st = as_stream(stream);
     if (cudaStreamSynchronize(st) != cudaSuccess) return USM_ERR_CUDA;

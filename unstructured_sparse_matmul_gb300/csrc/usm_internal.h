@@ -35,6 +35,8 @@ int launch_dense_transpose(const void* src, long long lds, int rows, int cols, b
                            long long ldd, cudaStream_t stream);
 int launch_row_softmax(int M, int nnz, const int* row_offsets, const float* scores, void* out, bool out_bf16,
                        cudaStream_t stream);
+int launch_csr_validate(int M, int K, int nnz, const int* row_offsets, const int* col_indices, int* result,
+                        cudaStream_t stream);
 
 // Stable LSD radix sort of item ids 0..n-1 by a key (8 bits per pass).
 enum class SortKey { RowSwizzle, Column };
