@@ -2,8 +2,8 @@
  * A plain C caller of the library's C ABI (include/usm.h): no C++, no Python.
  *
  * usage: usm_c_caller DIR
- * Reads DIR/problem.bin, runs row_swizzle_build, csr_spmm and csr_sddmm on
- * the GPU through the CUDA runtime, and writes DIR/C.bin (fp32 M×N) and
+ * Reads DIR/problem.bin, checks the CSR with csr_validate, runs
+ * row_swizzle_build, csr_spmm and csr_sddmm on the GPU through the CUDA runtime, and writes DIR/C.bin (fp32 M×N) and
  * DIR/out.bin (fp32 nnz).  problem.bin: int32 M, K, N, D, nnz; then
  * int32 row_offsets[M+1], int32 col_indices[nnz], float values[nnz],
  * float B[K·N], float X[M·D], float Y[K·D] (all row-major).
@@ -88,9 +88,22 @@ int main(int argc, char **argv) {
     cudaStream_t stream;
     if (cudaStreamCreate(&stream) != cudaSuccess) return fail("cudaStreamCreate", USM_ERR_CUDA);
 
+    int *d_check = to_device(NULL, sizeof(int) * USM_CSR_VALIDATE_INTS);
+    if (!d_check) return fail("cudaMalloc", USM_ERR_CUDA);
+    int st = csr_validate(M, K, nnz, d_ro, d_ci, d_check, stream);
+    if (st != USM_OK) return fail("csr_validate", st);
+    int check[2];
+    if (cudaMemcpyAsync(check, d_check, sizeof check, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return fail("csr_validate result", USM_ERR_CUDA);
+    if (check[0] != USM_CSR_VALID) {
+        fprintf(stderr, "usm_c_caller: CSR violates the contract (code %d at %d)\n", check[0], check[1]);
+        return 1;
+    }
+
     const size_t swz_bytes = row_swizzle_workspace_bytes(M, K);
     void *d_swz = to_device(NULL, swz_bytes);
-    int st = row_swizzle_build(M, K, 0, d_ro, d_perm, d_swz, swz_bytes, stream);
+    st = row_swizzle_build(M, K, 0, d_ro, d_perm, d_swz, swz_bytes, stream);
     if (st != USM_OK) return fail("row_swizzle_build", st);
 
     st = csr_spmm(M, K, N, nnz, d_ro, d_ci, d_vals, d_perm, 0, d_B, N, d_C, N, USM_F32, stream);
