@@ -29,6 +29,12 @@ MUTANTS = {
                                 "for (int32_t p = b; p < e; ++p) z += exp(s[p]);"),
     "bf16_ties_away": ("if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;",
                        "if (rem >= 0.5) fl += 1.0;"),
+    # CSR contract check.  (Dropping the row_offsets[M] = nnz rule is left
+    # out: the mutant would then read past the end of col_indices.)
+    "csr_check_allows_duplicates": ("if (p > ro[r] && ci[p] <= ci[p - 1]) return -6;",
+                                    "if (p > ro[r] && ci[p] < ci[p - 1]) return -6;"),
+    "csr_check_allows_K": ("if (ci[p] < 0 || ci[p] >= K) return -5;", "if (ci[p] < 0 || ci[p] > K) return -5;"),
+    "csr_check_ignores_decrease": ("if (ro[r + 1] < ro[r]) return -3;", "if (ro[r + 1] < ro[r] - 1000000) return -3;"),
 }
 
 
@@ -58,6 +64,7 @@ def pins_pass(golden_dir):
         lambda: T.test_sddmm_vs_dense_masked(64, 64, 64, 0.3),
         lambda: T.test_swizzle_vs_lexsort(1000, 300, 0),
         lambda: T.test_transpose_vs_dense(20, 30, 0.2),
+        lambda: T.test_csr_check_rejects_corruption(),
     ]
     for c in checks:
         try:
