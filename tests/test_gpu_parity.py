@@ -342,6 +342,32 @@ def test_bounded_wait_times_out_cleanly(usm):
     assert float(x.sum()) == 10.0
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_calls_leave_csr_untouched(usm, dtype):
+    """No call writes to the CSR arrays (or the swizzle, values and dense
+    operands) it is given: all compare equal byte for byte afterwards."""
+    import torch
+    M, K, N, D = 700, 900, 300, 300
+    csr = W.random_csr([M, K, 150], M, K, 0.1, dtype=dtype)
+    rng = np.random.default_rng(151)
+    B, X, Y = W.dense(rng, K, N, 1.0, dtype), W.dense(rng, M, D, 1.0, dtype), W.dense(rng, K, D, 1.0, dtype)
+    rod, cid, vd = csr_dev(csr)
+    Bd, Xd, Yd = dev(B, dtype), dev(X, dtype), dev(Y, dtype)
+    perm = usm.row_swizzle(rod, K, 350)
+    before = [t.clone() for t in (rod, cid, vd, Bd, Xd, Yd, perm)]
+    usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm, seg_rows=350)
+    s = usm.sddmm(rod, cid, Xd, Yd, row_swizzle=perm, seg_rows=350)
+    usm.sddmm_general(rod, cid, Xd, Yd, values=vd, row_swizzle=perm, seg_rows=350)
+    usm.row_softmax(rod, s)
+    usm.csr_transpose(rod, cid, vd, K, with_perm=True)
+    usm.csr_validate(rod, cid, K)
+    torch.cuda.synchronize()
+    for a, b in zip(before, (rod, cid, vd, Bd, Xd, Yd, perm)):
+        assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.uint8) if b.dtype == torch.bfloat16 else b)
+    assert usm.poll_status() == 0
+
+
 def test_misaligned_pointer_rejected(usm):
     import torch
     csr = W.random_csr(120, 10, 10, 0.3)
