@@ -163,6 +163,8 @@ def test_spmm_swizzle_does_not_change_bits(usm):
 SDDMM_SHAPES = [
     (1, 1, 1, 1.0), (7, 5, 3, 0.6), (37, 61, 64, 0.3), (130, 300, 129, 0.2), (257, 1000, 200, 0.1),
     (300, 129, 513, 0.05), (64, 2100, 128, 0.3), (1000, 50, 8, 0.9), (40, 70, 1000, 0.2),
+    # fp32 masks at least a quarter full take 256-wide strips: several, the last one ragged
+    (200, 500, 600, 0.3), (90, 2100, 300, 0.5),
 ]
 
 
@@ -182,10 +184,10 @@ def test_sddmm_small(usm, dtype, M, K, D, density, swz):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("D", [64, 128, 300])
-def test_sddmm_integer_valued_bit_exact(usm, dtype, D):
+@pytest.mark.parametrize("D,density", [(64, 0.2), (128, 0.2), (300, 0.2), (600, 0.3)])
+def test_sddmm_integer_valued_bit_exact(usm, dtype, D, density):
     M, K = 300, 700
-    csr = W.random_csr([M, K, 63], M, K, 0.2, dtype=dtype, int_valued=True)
+    csr = W.random_csr([M, K, 63], M, K, density, dtype=dtype, int_valued=True)
     rng = np.random.default_rng(64)
     X = W.dense(rng, M, D, 1.0, dtype, int_valued=True)
     Y = W.dense(rng, K, D, 1.0, dtype, int_valued=True)

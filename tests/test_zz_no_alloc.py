@@ -52,7 +52,7 @@ def test_static_scratch_matches_csr_sddmm_twice(usm, dtype):
 
 def test_static_scratch_rejects_oversized_problem(usm):
     lib = usm.load()
-    M, K, D = 64, 64, 4096          # 32 strips of 128
+    M, K, D = 4096, 4096, 4096      # a sparse mask (under 2% set): 32 strips of 128
     nnz = STATIC_SCRATCH_BYTES // (32 * 4) + 1
     assert lib.csr_sddmm_workspace_bytes(M, K, D, nnz, 0) > STATIC_SCRATCH_BYTES
     # Rejected on the host before any launch; the pointers are never read.

@@ -123,19 +123,22 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     return USM_OK;
 }
 
-// Strip width by element type and D: fp32 strips are 128 wide (8 lanes x 16
-// values), bf16 strips 128 wide, or 64 when D ≤ 64.  256-wide strips (half
-// the partials) measured 3-7% faster at 70% sparsity on the FFN shapes but
-// 7-24% slower at 90-95%.
-int strip_width(int D, bool bf16) { return (bf16 && D <= 64) ? 64 : 128; }
+// Strip width by element type, density and D.  fp32: 256 wide (8 lanes x 32
+// values) when at least a quarter of the mask is set, else 128 (8 x 16):
+// wider strips halve the partials and the list work per FMA but double the
+// work per (row, chunk), which dominates at high sparsity (measured on the
+// FFN shapes, 256 against 128: 4-6% faster at 70% sparsity, -2..+2% at 80%,
+// 3-11% slower at 90-95%).  bf16: 128 wide, or 64 when D <= 64.
+int strip_width(int M, int K, int D, int nnz, bool bf16) {
+    if (bf16) return D <= 64 ? 64 : 128;
+    return 4LL * nnz >= (long long)M * K ? 256 : 128;
+}
 
 }  // namespace
 
 size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16) {
-    (void)M;
-    (void)K;
     if (D <= 0 || nnz <= 0) return 0;
-    const int dt = strip_width(D, bf16);
+    const int dt = strip_width(M, K, D, nnz, bf16);
     const long long nstrips = (D + dt - 1) / dt;
     return nstrips > 1 ? (size_t)nstrips * (size_t)nnz * sizeof(float) : 0;
 }
@@ -169,8 +172,13 @@ int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream) {
 int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, size_t ws_bytes,
                  cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SDDMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
-    // fp32: one CTA per SM, up to 128 registers, one 192 KB stage (KC = 384).
-    if (!in_bf16) return launch_cfg<false, 8, 4, W, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
+    // fp32: one CTA per SM, up to 128 registers, one 192 KB stage (KC = 384
+    // rows of a 128-wide strip, or 192 of a 256-wide one).
+    if (!in_bf16) {
+        if (strip_width(a.M, a.K, a.D, a.nnz, false) == 256)
+            return launch_cfg<false, 8, 8, W, 96 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
+        return launch_cfg<false, 8, 4, W, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
+    }
     if (a.D <= 64) return launch_cfg<true, 8, 1, W, 384 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
     return launch_cfg<true, 8, 2, W, 192 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
 }
