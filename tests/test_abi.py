@@ -62,11 +62,12 @@ def test_workspace_sizes(lib):
     assert lib.csr_sddmm_workspace_bytes(10, 10, 64, 100, usm.USM_F32) == 0        # one strip
     assert lib.csr_sddmm_workspace_bytes(10, 10, 128, 100, usm.USM_F32) == 0
     assert lib.csr_sddmm_workspace_bytes(100, 10, 129, 100, usm.USM_F32) == 2 * 100 * 4  # 128-wide strips
-    # fp32 masks at least a quarter full use 256-wide strips
+    # masks at least a quarter full use 256-wide strips (bf16 too, unless D <= 64)
     assert lib.csr_sddmm_workspace_bytes(10, 10, 129, 100, usm.USM_F32) == 0
     assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 25, usm.USM_F32) == 2 * 25 * 4
     assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 24, usm.USM_F32) == 3 * 24 * 4
-    assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 100, usm.USM_BF16) == 3 * 100 * 4  # bf16: 128
+    assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 100, usm.USM_BF16) == 2 * 100 * 4
+    assert lib.csr_sddmm_workspace_bytes(100, 10, 257, 100, usm.USM_BF16) == 3 * 100 * 4
     assert lib.csr_sddmm_workspace_bytes(10, 10, 2048, 7, usm.USM_BF16) == 16 * 7 * 4
     assert lib.csr_sddmm_workspace_bytes(10, 10, 64, 7, usm.USM_BF16) == 0
     assert lib.csr_sddmm_workspace_bytes(10, 10, 0, 7, usm.USM_F32) == 0

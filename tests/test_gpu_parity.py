@@ -163,7 +163,7 @@ def test_spmm_swizzle_does_not_change_bits(usm):
 SDDMM_SHAPES = [
     (1, 1, 1, 1.0), (7, 5, 3, 0.6), (37, 61, 64, 0.3), (130, 300, 129, 0.2), (257, 1000, 200, 0.1),
     (300, 129, 513, 0.05), (64, 2100, 128, 0.3), (1000, 50, 8, 0.9), (40, 70, 1000, 0.2),
-    # fp32 masks at least a quarter full take 256-wide strips: several, the last one ragged
+    # masks at least a quarter full take 256-wide strips: several, the last one ragged
     (200, 500, 600, 0.3), (90, 2100, 300, 0.5),
 ]
 

@@ -123,14 +123,15 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     return USM_OK;
 }
 
-// Strip width by element type, density and D.  fp32: 256 wide (8 lanes x 32
-// values) when at least a quarter of the mask is set, else 128 (8 x 16):
-// wider strips halve the partials and the list work per FMA but double the
-// work per (row, chunk), which dominates at high sparsity (measured on the
-// FFN shapes, 256 against 128: 4-6% faster at 70% sparsity, -2..+2% at 80%,
-// 3-11% slower at 90-95%).  bf16: 128 wide, or 64 when D <= 64.
+// Strip width by density, element type and D: 256 columns when at least a
+// quarter of the mask is set, else 128 (bf16 with D <= 64: 64).  Wider strips
+// halve the partials and the list work per FMA but double the work per (row,
+// chunk), which dominates at high sparsity.  Measured on the FFN shapes, 256
+// against 128: fp32 4-6% faster at 70% sparsity, -2..+2% at 80%, 3-11%
+// slower at 90-95%; bf16 0-7% faster at 70%, -5..+2% at 80-90%, 9-13%
+// slower at 95%.
 int strip_width(int M, int K, int D, int nnz, bool bf16) {
-    if (bf16) return D <= 64 ? 64 : 128;
+    if (bf16 && D <= 64) return 64;
     return 4LL * nnz >= (long long)M * K ? 256 : 128;
 }
 
@@ -180,6 +181,8 @@ int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, si
         return launch_cfg<false, 8, 4, W, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
     }
     if (a.D <= 64) return launch_cfg<true, 8, 1, W, 384 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
+    if (strip_width(a.M, a.K, a.D, a.nnz, true) == 256)
+        return launch_cfg<true, 8, 4, W, 96 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
     return launch_cfg<true, 8, 2, W, 192 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);
 }
 
