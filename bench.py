@@ -318,6 +318,8 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if wl in FLUSH_L2 else None
 
     def step(events=None):
+        """One pass over the launch list on one stream, optionally with
+        events around every call."""
         if flush is not None:
             flush.zero_()
         for i, (label, op, d) in enumerate(launches):
@@ -327,13 +329,44 @@ def run_ours(args, rank, world, local_rank):
             if events is not None:
                 events[i][1].record(stream)
 
+    # The step's problems are independent (own outputs and workspaces): they
+    # are dealt round-robin over `streams` compute streams, each problem's
+    # calls in order on its stream, so one call's last wave of CTAs overlaps
+    # the next problem's first.
+    groups = []
+    for label, op, d in launches:
+        if not groups or groups[-1][0] is not d:
+            groups.append((d, []))
+        groups[-1][1].append(op)
+    n_streams = max(1, min(args.streams, len(groups)))
+    concurrent = n_streams > 1 and flush is None and wl not in GRAPHED
+    cstreams = [torch.cuda.Stream(device=dev) for _ in range(n_streams)] if concurrent else []
+    fork = torch.cuda.Event()
+    joins = [torch.cuda.Event() for _ in cstreams]
+
+    def step_streams():
+        fork.record(stream)
+        for cs in cstreams:
+            cs.wait_event(fork)
+        for j, (d, ops) in enumerate(groups):
+            with torch.cuda.stream(cstreams[j % n_streams]):
+                for op in ops:
+                    run_one(op, d)
+        for cs, e in zip(cstreams, joins):
+            e.record(cs)
+            stream.wait_event(e)
+
     for _ in range(args.warmup):
         step()
+        if concurrent:
+            step_streams()
     torch.cuda.synchronize()
     if usm.poll_status() != 0:
         raise RuntimeError("device status word set during warm-up")
 
-    # Timed region: K steps, per-launch events on the launching stream.
+    # Timed regions: (1) K steps on the compute streams (the step's time);
+    # (2) K steps on one stream with events around every call (per-launch
+    # durations and the roofline, free of overlap).  Clocks sampled across both.
     ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in launches]
           for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -343,6 +376,13 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
+    if concurrent:
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for k in range(args.steps):
+            step_streams()
+        c1.record(stream)
+        torch.cuda.synchronize()
     start.record(stream)
     for k in range(args.steps):
         step(ev[k])
@@ -351,7 +391,8 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    elapsed_ms = start.elapsed_time(stop)
+    one_stream_ms = start.elapsed_time(stop)
+    elapsed_ms = c0.elapsed_time(c1) if concurrent else one_stream_ms
     if usm.poll_status() != 0:
         raise RuntimeError("device status word set during the timed region")
     per_launch_ms = {label: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
@@ -383,7 +424,9 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError("device status word set during the graph replays")
     if flush is not None or wl in GRAPHED:  # time the launches alone
         elapsed_ms = sum(per_launch_ms.values()) * args.steps
+        one_stream_ms = elapsed_ms
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    one_stream_ms = max_over_ranks(one_stream_ms, world, dev)
 
     step_flops = sum(flops_of(d["p"], op) for _, op, d in launches)
     step_bytes = sum(alg_bytes(d["p"], op) for _, op, d in launches)
@@ -410,7 +453,7 @@ def run_ours(args, rank, world, local_rank):
     traffic = recorded_traffic(dom_label)
 
     # End to end through the public API with host buffers.
-    e2e = run_e2e(args, usm, torch, dev, launches, step_flops) if not args.no_e2e and wl == "ffn" else None
+    e2e = run_e2e(args, usm, torch, dev, launches, step_flops, n_streams) if not args.no_e2e and wl == "ffn" else None
 
     result = {
         "metric": "SpMM/SDDMM useful GFLOP/s (2·nnz·N), HBM GB/s, % of roofline on 1 GB300",
@@ -420,6 +463,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "ms_per_step_one_stream": round(one_stream_ms / args.steps, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -434,6 +478,10 @@ def run_ours(args, rank, world, local_rank):
                           f"warm L2 (0.2 MB problem); each call timed in a CUDA graph of {GRAPH_CALLS} calls"
                           if wl in GRAPHED else "inputs larger than L2: each step's operands exceed 129 MB"),
                    "swizzle": "row swizzle built once per pattern before timing",
+                   "streams": (f"{n_streams} compute streams, problems dealt round-robin, each problem's calls "
+                               "in order on its stream; per-launch table and roofline from a second timed pass "
+                               "on one stream with events around every call" if concurrent
+                               else "one stream, events around every call"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm_alg_gbs": round(step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9, 1),
         "roofline_frac_step": round(value / 1e3 / (FP32_PEAK_TFLOPS * world), 4),
@@ -496,16 +544,18 @@ def recorded_traffic(label):
     return None
 
 
-def run_e2e(args, usm, torch, dev, launches, step_flops):
+def run_e2e(args, usm, torch, dev, launches, step_flops, n_streams=1):
     """Same metric through the API with host buffers: every step copies the
     step's inputs from pinned host memory and reads the results back.
 
     The copies are pipelined against the kernels the way a caller feeding the
     library from host memory would: uploads on one stream, the library calls
-    on the compute stream, downloads on a third, problem by problem, with
-    events so that problem i's kernels start once its own inputs have landed
-    and a step never overwrites buffers the previous step still reads."""
-    comp = torch.cuda.current_stream()
+    on the compute streams (problems dealt round-robin, as in the device-side
+    step), downloads on another, problem by problem, with events so that
+    problem i's kernels start once its own inputs have landed and a step never
+    overwrites buffers the previous step still reads."""
+    main = torch.cuda.current_stream()
+    comps = [torch.cuda.Stream(device=dev) for _ in range(max(1, n_streams))]
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     order, per = [], {}
     for label, op, d in launches:
@@ -522,8 +572,9 @@ def run_e2e(args, usm, torch, dev, launches, step_flops):
     ev = {k: {n: torch.cuda.Event() for n in ("in", "comp", "out")} for k in order}
 
     def e2e_step(serial=False):
-        for k in order:
+        for j, k in enumerate(order):
             item, e = per[k], ev[k]
+            comp = comps[0] if serial else comps[j % len(comps)]
             if serial:  # no overlap: each upload waits for the previous download
                 comp.wait_stream(down)
                 up.wait_stream(comp)
@@ -556,14 +607,14 @@ def run_e2e(args, usm, torch, dev, launches, step_flops):
             e2e_step(serial)
         torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(comp)
-        up.wait_event(s0)
-        down.wait_event(s0)
+        s0.record(main)
+        for st in comps + [up, down]:
+            st.wait_event(s0)
         for _ in range(steps):
             e2e_step(serial)
-        comp.wait_stream(up)
-        comp.wait_stream(down)
-        s1.record(comp)
+        for st in comps + [up, down]:
+            main.wait_stream(st)
+        s1.record(main)
         torch.cuda.synchronize()
         return step_flops * steps / (s0.elapsed_time(s1) * 1e-3) / 1e9
 
@@ -571,7 +622,7 @@ def run_e2e(args, usm, torch, dev, launches, step_flops):
     serial = timed(True)
     return {"value": round(value, 1), "unit": "GFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "overlap": "uploads, kernels and downloads on three streams, pipelined problem by problem",
+            "overlap": f"uploads, kernels ({len(comps)} compute streams) and downloads pipelined problem by problem",
             "serial_value": round(serial, 1)}
 
 
@@ -659,6 +710,8 @@ def main():
                     help="row fraction of each launch the cpu_baseline oracle computes (6 passes)")
     ap.add_argument("--ref-sample", type=float, default=0.25,
                     help="row fraction of each launch per step of the --impl reference arm")
+    ap.add_argument("--streams", type=int, default=3,
+                    help="compute streams the step's independent problems are dealt over (1: one stream)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="ffn", choices=sorted(WORKLOADS),
