@@ -370,6 +370,45 @@ def test_calls_leave_csr_untouched(usm, dtype):
     assert usm.poll_status() == 0
 
 
+def test_concurrent_streams_match_one_stream(usm):
+    """Independent problems dealt over three streams at once (as the bench
+    runs its step) give the same bits as the same calls on one stream: the
+    kernels keep no state outside their arguments."""
+    import torch
+    probs = []
+    for i, (M, K, dt, dens) in enumerate([(600, 900, "f32", 0.3), (900, 600, "bf16", 0.1), (400, 1500, "f32", 0.05),
+                                          (700, 700, "bf16", 0.3), (500, 800, "f32", 0.2), (300, 2000, "bf16", 0.25)]):
+        csr = W.random_csr([M, K, 170 + i], M, K, dens, dtype=dt)
+        rng = np.random.default_rng(180 + i)
+        N = 300
+        d = dict(csr=csr, dt=dt, K=K, B=dev(W.dense(rng, K, N, 1.0, dt), dt), X=dev(W.dense(rng, M, N, 1.0, dt), dt),
+                 Y=dev(W.dense(rng, K, N, 1.0, dt), dt))
+        d["ro"], d["ci"], d["v"] = csr_dev(csr)
+        d["perm"] = usm.row_swizzle(d["ro"], K)
+        probs.append(d)
+
+    def run_all(streams):
+        outs = [None] * len(probs)
+        main = torch.cuda.current_stream()
+        for s in streams:
+            s.wait_stream(main)
+        for j, d in enumerate(probs):
+            with torch.cuda.stream(streams[j % len(streams)]):
+                C = usm.spmm(d["ro"], d["ci"], d["v"], d["B"], K=d["K"], row_swizzle=d["perm"])
+                S = usm.sddmm(d["ro"], d["ci"], d["X"], d["Y"], row_swizzle=d["perm"])
+                outs[j] = (C, S)
+        for s in streams:
+            main.wait_stream(s)
+        torch.cuda.synchronize()
+        return [(host(C), host(S)) for C, S in outs]
+
+    one = run_all([torch.cuda.current_stream()])
+    many = run_all([torch.cuda.Stream() for _ in range(3)])
+    for j, ((c1, s1), (c3, s3)) in enumerate(zip(one, many)):
+        assert np.array_equal(c1, c3) and np.array_equal(s1, s3), j
+    assert usm.poll_status() == 0
+
+
 def test_misaligned_pointer_rejected(usm):
     import torch
     csr = W.random_csr(120, 10, 10, 0.3)
