@@ -160,6 +160,31 @@ __global__ void __launch_bounds__(W * 32, MINB)
     const int strip = blockIdx.y;
     const int d0 = strip * C_::DT;
 
+    // The tile's chunks [c_lo, c_lo + nchunks) are split into gridDim.z
+    // contiguous ranges, one per CTA on z: every nonzero falls in exactly one.
+    // With one diagonal block the tile's span is all of K, known before any
+    // load, so the first copy starts at once and the row look-ups overlap it;
+    // block-diagonal schedules first find the tile's column range.
+    const bool whole = a.seg_rows >= a.M;
+    int c_lo = 0, nchunks = 0;
+    auto split = [&](int lo, int hi) {  // columns [lo, hi] of the tile, hi >= lo
+        const int per = (hi / KC - lo / KC + 1 + gridDim.z - 1) / gridDim.z;
+        const int first = lo / KC + blockIdx.z * per;
+        c_lo = first;
+        nchunks = max(0, min(hi / KC + 1, first + per) - first);
+    };
+    if (whole && a.K > 0) split(0, a.K - 1);
+    auto issue = [&](int j) {
+        const int s = j % NS;
+        const uint32_t bar = smem_addr(&bars[s]);
+        mbar_arrive_expect_tx(bar, STAGE);
+        const uint32_t dst = smem_addr(stages + s * STAGE);
+#pragma unroll
+        for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
+            tma_load_2d(dst + b * C_::BOX_ROWS * PITCH, &tmY, d0, (c_lo + j) * KC + b * C_::BOX_ROWS,
+                        bar);
+    };
+
     if (threadIdx.x == 0) {
         kr[0] = INT_MAX;
         kr[1] = -1;
@@ -168,6 +193,10 @@ __global__ void __launch_bounds__(W * 32, MINB)
         mbar_init(smem_addr(&bars[1]), 1);
         fence_barrier_init();
         prefetch_tensor_map(&tmY);
+        if (whole) {
+            if (nchunks > 0) issue(0);
+            if (NS > 1 && nchunks > 1) issue(1);
+        }
     }
 
     int my_row = -1, my_start = 0, my_end = 0;
@@ -185,52 +214,35 @@ __global__ void __launch_bounds__(W * 32, MINB)
             }
         }
     }
-    int kmin = INT_MAX, kmax = -1;
-    if (my_end > my_start) {
-        kmin = __ldg(a.col_indices + my_start);
-        kmax = __ldg(a.col_indices + my_end - 1);
-    }
+    if (whole) {
+        __syncthreads();  // barrier and flag initialisation visible to every thread
+    } else {
+        int kmin = INT_MAX, kmax = -1;
+        if (my_end > my_start) {
+            kmin = __ldg(a.col_indices + my_start);
+            kmax = __ldg(a.col_indices + my_end - 1);
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        kmin = min(kmin, __shfl_xor_sync(kFullMask, kmin, o));
-        kmax = max(kmax, __shfl_xor_sync(kFullMask, kmax, o));
-    }
-    __syncthreads();
-    if (lane == 0 && kmax >= 0) {
-        atomicMin(&kr[0], kmin);
-        atomicMax(&kr[1], kmax);
-    }
-    __syncthreads();
-    // The tile's chunks [c_lo, c_lo + nchunks) are split into gridDim.z
-    // contiguous ranges, one per CTA on z: every nonzero falls in exactly one.
-    int c_lo = 0, nchunks = 0;
-    {
+        for (int o = 16; o > 0; o >>= 1) {
+            kmin = min(kmin, __shfl_xor_sync(kFullMask, kmin, o));
+            kmax = max(kmax, __shfl_xor_sync(kFullMask, kmax, o));
+        }
+        __syncthreads();
+        if (lane == 0 && kmax >= 0) {
+            atomicMin(&kr[0], kmin);
+            atomicMax(&kr[1], kmax);
+        }
+        __syncthreads();
         const int lo = max(kr[0], 0), hi = min(kr[1], a.K - 1);
-        if (kr[1] >= 0 && lo <= hi) {
-            const int per = (hi / KC - lo / KC + 1 + gridDim.z - 1) / gridDim.z;
-            const int first = lo / KC + blockIdx.z * per;
-            c_lo = first;
-            nchunks = max(0, min(hi / KC + 1, first + per) - first);
+        if (kr[1] >= 0 && lo <= hi) split(lo, hi);
+        if (threadIdx.x == 0) {
+            if (nchunks > 0) issue(0);
+            if (NS > 1 && nchunks > 1) issue(1);
         }
     }
     // Later ranges start each row at its first nonzero in range (binary search
     // of the sorted column indices; lanes < R, overlapping the first copy).
     const bool later = blockIdx.z > 0 && nchunks > 0;
-
-    auto issue = [&](int j) {
-        const int s = j % NS;
-        const uint32_t bar = smem_addr(&bars[s]);
-        mbar_arrive_expect_tx(bar, STAGE);
-        const uint32_t dst = smem_addr(stages + s * STAGE);
-#pragma unroll
-        for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
-            tma_load_2d(dst + b * C_::BOX_ROWS * PITCH, &tmY, d0, (c_lo + j) * KC + b * C_::BOX_ROWS,
-                        bar);
-    };
-    if (threadIdx.x == 0) {
-        if (nchunks > 0) issue(0);
-        if (NS > 1 && nchunks > 1) issue(1);
-    }
     if (later && my_end > my_start) {
         const int k_first = c_lo * KC;
         int lo = my_start, hi = my_end;  // first position with column >= k_first

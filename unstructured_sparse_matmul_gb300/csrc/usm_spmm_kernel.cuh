@@ -18,9 +18,10 @@
 // * Dense operand staging.  The CTA walks K in chunks of KC rows.  For each
 //   chunk one thread issues TMA tensor copies of B[k0:k0+KC, n0:n0+NT] into a
 //   shared-memory stage (completion on an mbarrier, bounded wait; one or two
-//   stages).  Only the chunks between the smallest and largest column index of
-//   the CTA's rows are fetched, so block-diagonal (batched) matrices stay
-//   cheap.
+//   stages).  Under a block-diagonal schedule only the chunks between the
+//   smallest and largest column index of the CTA's rows are fetched, so
+//   batched matrices stay cheap; with one block the CTA walks all of K and
+//   starts its first copy before looking its rows up.
 // * Sparse operand.  For each (row, chunk) a warp reads the next 32 column
 //   indices and values of the row with coalesced loads (the window after the
 //   row's cursor, so a misaligned row start costs nothing), keeps the prefix
@@ -138,6 +139,25 @@ __global__ void __launch_bounds__(W * 32, MB)
     const int n0 = blockIdx.y * C_::NT;
     const int tile = blockIdx.x;
 
+    // With one diagonal block every tile may touch any column: the chunk range
+    // is all of K, known before any load, so the first copy starts at once and
+    // the row look-ups below overlap it.  Block-diagonal schedules first find
+    // the tile's column range (a block touches only its own columns).
+    const bool whole = a.seg_rows >= a.M;
+    int c_lo = 0, nchunks = whole ? (a.K + KC - 1) / KC : 0;
+    auto issue = [&](int j) {
+        const int s = j % NS;
+        const uint32_t bar = smem_addr(&bars[s]);
+        mbar_arrive_expect_tx(bar, STAGE);
+        const uint32_t dst = smem_addr(stages + s * STAGE);
+#pragma unroll
+        for (int x = 0; x < C_::NBOX; ++x)
+#pragma unroll
+            for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
+                tma_load_2d(dst + x * C_::BOX_BYTES + b * C_::BOX_ROWS * PITCH, &tmB, n0 + x * C_::BOX_COLS,
+                            (c_lo + j) * KC + b * C_::BOX_ROWS, bar);
+    };
+
     if (threadIdx.x == 0) {
         kr[0] = INT_MAX;
         kr[1] = -1;
@@ -146,6 +166,10 @@ __global__ void __launch_bounds__(W * 32, MB)
         mbar_init(smem_addr(&bars[1]), 1);
         fence_barrier_init();
         prefetch_tensor_map(&tmB);
+        if (whole) {
+            if (nchunks > 0) issue(0);
+            if (NS > 1 && nchunks > 1) issue(1);
+        }
     }
 
     // Row slots of this warp: slot i is row perm[tile*MT + i*W + warp].
@@ -164,46 +188,34 @@ __global__ void __launch_bounds__(W * 32, MB)
             }
         }
     }
-    int kmin = INT_MAX, kmax = -1;
-    if (my_end > my_start) {
-        kmin = __ldg(a.col_indices + my_start);
-        kmax = __ldg(a.col_indices + my_end - 1);
-    }
+    if (whole) {
+        __syncthreads();  // barrier and flag initialisation visible to every thread
+    } else {
+        int kmin = INT_MAX, kmax = -1;
+        if (my_end > my_start) {
+            kmin = __ldg(a.col_indices + my_start);
+            kmax = __ldg(a.col_indices + my_end - 1);
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        kmin = min(kmin, __shfl_xor_sync(kFullMask, kmin, o));
-        kmax = max(kmax, __shfl_xor_sync(kFullMask, kmax, o));
-    }
-    __syncthreads();
-    if (lane == 0 && kmax >= 0) {
-        atomicMin(&kr[0], kmin);
-        atomicMax(&kr[1], kmax);
-    }
-    __syncthreads();
-    int c_lo = 0, nchunks = 0;
-    {
+        for (int o = 16; o > 0; o >>= 1) {
+            kmin = min(kmin, __shfl_xor_sync(kFullMask, kmin, o));
+            kmax = max(kmax, __shfl_xor_sync(kFullMask, kmax, o));
+        }
+        __syncthreads();
+        if (lane == 0 && kmax >= 0) {
+            atomicMin(&kr[0], kmin);
+            atomicMax(&kr[1], kmax);
+        }
+        __syncthreads();
         const int lo = max(kr[0], 0), hi = min(kr[1], a.K - 1);
         if (kr[1] >= 0 && lo <= hi) {
             c_lo = lo / KC;
             nchunks = hi / KC - c_lo + 1;
         }
-    }
-
-    auto issue = [&](int j) {
-        const int s = j % NS;
-        const uint32_t bar = smem_addr(&bars[s]);
-        mbar_arrive_expect_tx(bar, STAGE);
-        const uint32_t dst = smem_addr(stages + s * STAGE);
-#pragma unroll
-        for (int x = 0; x < C_::NBOX; ++x)
-#pragma unroll
-            for (int b = 0; b < KC / C_::BOX_ROWS; ++b)
-                tma_load_2d(dst + x * C_::BOX_BYTES + b * C_::BOX_ROWS * PITCH, &tmB, n0 + x * C_::BOX_COLS,
-                            (c_lo + j) * KC + b * C_::BOX_ROWS, bar);
-    };
-    if (threadIdx.x == 0) {
-        if (nchunks > 0) issue(0);
-        if (NS > 1 && nchunks > 1) issue(1);
+        if (threadIdx.x == 0) {
+            if (nchunks > 0) issue(0);
+            if (NS > 1 && nchunks > 1) issue(1);
+        }
     }
 
     float acc[R][VEC];
