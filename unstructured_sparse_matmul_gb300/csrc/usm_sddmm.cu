@@ -49,16 +49,17 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     // model fitted to a sweep of the FFN launches (R ∈ {4..32}, every
     // effective S, T the fewest tiles or the most that still fit in the same
     // number of CTA waves; L2 flushed between calls; the model's choices sum
-    // to 1.2% above the best per launch).  Time = waves × per-CTA work, with
-    // waves = ceil(CTAs / resident slots): CTAs of a launch have near-equal
-    // work (swizzled rows), so a part-filled last wave costs a whole one and
-    // more, shorter tiles that fill it are free.  Work is counted in units of
-    // one consumed row: staging the CTA's share of the K span (0.45 a row),
-    // its share of the tile's rows, a fixed start-up (6000: first copy,
-    // cursor search, epilogue) and a latency per (row, chunk) that a warp's
-    // rows pay one after another (880).  Splitting K costs no reduction
-    // (each nonzero belongs to one split); only split counts that give every
-    // split a different chunk range are tried.
+    // to 1.2% above the best per launch on 128-wide strips, 2% on 256-wide
+    // ones).  Time = waves × per-CTA work, with waves = ceil(CTAs / resident
+    // slots): CTAs of a launch have near-equal work (swizzled rows), so a
+    // part-filled last wave costs a whole one and more, shorter tiles that
+    // fill it are free.  Work is counted in consumed nonzeros: staging the
+    // CTA's share of the K span (0.45 a staged row), the nonzeros of its rows
+    // in its share of the span, a fixed start-up (6000: first copy, cursor
+    // search, epilogue) and a latency per (row, chunk) that a warp's rows pay
+    // one after another (880).  Splitting K costs no reduction (each nonzero
+    // belongs to one split); only split counts that give every split a
+    // different chunk range are tried.
     int R = 1, S = 1, T = 1;
     {
         double best = 0.0;
