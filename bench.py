@@ -494,6 +494,11 @@ def run_ours(args, rank, world, local_rank):
                                        "source": "shared-memory delivery 125 B/clk/SM (probe), one dense "
                                                  "element per useful FMA"}},
         "setup": {"row_swizzle_ms_all_patterns": round(swz_ms, 4), "patterns": len(items)},
+        # Measured character of every generated matrix (sparsity within its
+        # diagonal block, mean row length, row-length CoV).
+        "matrices": [dict({"name": d["p"].name},
+                          **{k: (round(v, 4) if isinstance(v, float) else v) for k, v in W.stats(d["p"].csr).items()})
+                     for d in items],
         "per_launch": rows,
         "gpu_launches": sum(kernels_per_launch[label] for label, _, _ in launches) * args.steps
                         * (GRAPH_CALLS if wl in GRAPHED else 1),
