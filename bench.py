@@ -496,7 +496,7 @@ def run_ours(args, rank, world, local_rank):
         "setup": {"row_swizzle_ms_all_patterns": round(swz_ms, 4), "patterns": len(items)},
         # Measured character of every generated matrix (sparsity within its
         # diagonal block, mean row length, row-length CoV).
-        "matrices": [dict({"name": d["p"].name},
+        "matrices": [dict({"name": d["p"].name, "dtype": d["p"].dtype},
                           **{k: (round(v, 4) if isinstance(v, float) else v) for k, v in W.stats(d["p"].csr).items()})
                      for d in items],
         "per_launch": rows,
