@@ -32,20 +32,36 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 N_FFN = 2048
-SMS = 152
 FP32_LANES_PER_SM = 128
-SM_MAX_MHZ = 2070.0
-# FP32 CUDA-core peak: 152 SMs x 128 FMA lanes x 2 flop x 2.07 GHz.
-FP32_PEAK_TFLOPS = SMS * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ * 1e6 / 1e12
+SM_MAX_MHZ_DEFAULT = 2070.0  # GB300's maximum SM clock, when nothing better is known
 # On-chip operand delivery: every useful FMA reads one dense-operand element
 # from shared memory that no other FMA of its lane reuses, and shared memory
-# delivered 125 B/clk/SM to 128-bit loads (probe on GB300): at most
-# 125/4 fp32 (125/2 bf16) FMAs per clock per SM.
+# delivers 125 B/clk/SM to 128-bit loads at random staged rows (measured on
+# GB300: profiles/operand_bound.md): at most 125/4 fp32 (125/2 bf16) FMAs per
+# clock per SM.
 SMEM_BYTES_PER_CLK = 125.0
 
 
+class Device:
+    """The SM count and maximum SM clock the roofline figures use: read from
+    the device (and MEASURED_PEAKS.json's sm_max_mhz) when a GPU is present."""
+    sms = 152
+    sm_max_mhz = SM_MAX_MHZ_DEFAULT
+
+    @classmethod
+    def probe(cls, index=0):
+        import torch
+        cls.sms = torch.cuda.get_device_properties(index).multi_processor_count
+        cls.sm_max_mhz = float((measured_peaks() or {}).get("sm_max_mhz", SM_MAX_MHZ_DEFAULT))
+
+
+def fp32_peak_tflops():
+    """FP32 CUDA-core peak: SMs x 128 FMA lanes x 2 flop x the maximum SM clock."""
+    return Device.sms * FP32_LANES_PER_SM * 2 * Device.sm_max_mhz * 1e6 / 1e12
+
+
 def operand_bound_tflops(elem_bytes):
-    return SMS * SMEM_BYTES_PER_CLK / elem_bytes * 2 * SM_MAX_MHZ * 1e6 / 1e12
+    return Device.sms * SMEM_BYTES_PER_CLK / elem_bytes * 2 * Device.sm_max_mhz * 1e6 / 1e12
 WORKLOAD = ("transformer_ffn: A 4096x1024 and 1024x4096 at 70/80/90/95% sparsity (row lengths "
             "N(mu, (0.1mu)^2), uniform columns, values N(0,0.02)); SpMM forward with B Kx2048 and "
             "SDDMM weight-gradient with X Mx2048, Y Kx2048, N(0,1); fp32 and bf16-in/fp32-acc")
@@ -225,6 +241,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    Device.probe(local_rank)
+    FP32_PEAK_TFLOPS = fp32_peak_tflops()
     usm.load()
     stream = torch.cuda.current_stream()
 
@@ -467,7 +485,8 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": ("f32 + bf16-in/fp32-acc" if len({d["p"].dtype for d in items}) > 1
+                  else "f32" if items[0]["p"].dtype == "f32" else "bf16-in/fp32-acc"),
         "data": "synthetic (seeded, shaped like the pages' " + ("Transformer-FFN weights)" if wl.startswith("ffn")
                                                                 else f"{wl} workload)"),
         "config": {"workload": (WORKLOAD if wl == "ffn" else f"{wl}: {WORKLOADS[wl]}")
@@ -488,11 +507,12 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "alu", "achieved": dom["tflops"], "peak": round(FP32_PEAK_TFLOPS, 2),
                      "unit": "TFLOP/s", "frac": round(dom["tflops"] / FP32_PEAK_TFLOPS, 4),
                      "traffic": traffic, "kernel": dom_label,
-                     "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz",
+                     "peak_source": f"derived: {Device.sms} SMs x 128 FP32 lanes x 2 flop x "
+                                    f"{Device.sm_max_mhz / 1e3:.3g} GHz",
                      "operand_bound": {"peak": round(operand_bound_tflops(2 if "bf16" in dom_label else 4), 2),
                                        "frac": dom["frac_operand_bound"],
-                                       "source": "shared-memory delivery 125 B/clk/SM (probe), one dense "
-                                                 "element per useful FMA"}},
+                                       "source": "shared-memory delivery 125 B/clk/SM (profiles/operand_bound.md), "
+                                                 "one dense element per useful FMA"}},
         "setup": {"row_swizzle_ms_all_patterns": round(swz_ms, 4), "patterns": len(items)},
         # Measured character of every generated matrix (sparsity within its
         # diagonal block, mean row length, row-length CoV).
@@ -705,6 +725,18 @@ def run_reference(args, rank, world):
     }
 
 
+def relaunch_under_torchrun(n):
+    """Run this script again as n ranks on this node (127.0.0.1, a free
+    port); returns the launcher's exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd, env=dict(os.environ, MASTER_ADDR="127.0.0.1"))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -728,9 +760,17 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
 
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be at least 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # One process per GPU: start the N ranks under torch.distributed.run
+        # (the same launch the multi-GPU runs use) and pass its status on.
+        raise SystemExit(relaunch_under_torchrun(args.gpus))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU")
 
     if args.impl == "reference":
         res = run_reference(args, rank, world)

@@ -33,7 +33,9 @@
  *   throws, aborts or prints.  Argument checks run on the host before any
  *   launch, so a rejected call touches no device memory.
  * Threads.  Calls may be issued from several host threads; the status word
- *   is shared by all calls on one device.
+ *   is shared by all calls on one device.  The library keeps the device
+ *   address of that word (and of csr_sddmm_static_scratch's array) per device
+ *   and per CUDA context, and looks it up again after a device reset.
  */
 #ifndef USM_H_
 #define USM_H_
@@ -128,22 +130,31 @@ int csr_sddmm(int M, int K, int D, int nnz,
  * environment that forbids allocation after initialisation) and so cannot
  * supply csr_sddmm's workspace.  Same arguments, contract and result as
  * csr_sddmm, minus the workspace: the scratch comes from one fixed 32 MiB
- * array in the library's device image, which every GPU that loads the
- * library holds until the process exits.
+ * array in the library's device image.
  *
  *   Limit: csr_sddmm_workspace_bytes(M, K, D, nnz, in_dtype) must not exceed
  *          32 MiB (33554432 bytes); larger problems return USM_ERR_UNSUPPORTED
  *          before anything is launched.  Problems that need no workspace
- *          (one column strip) always fit.
- *   Allocation: none, on any call (no cudaMalloc, cudaFree or allocating
+ *          (one column strip) always fit and never touch the array.
+ *   Set-up: the first call on a device that needs the array (with that
+ *          device current) looks up its device address with
+ *          cudaGetSymbolAddress.  CUDA loads the library's device code
+ *          lazily, so this first call may also load the module that holds
+ *          the array and reserve its 32 MiB on that device; it returns
+ *          USM_ERR_CUDA if the device has no room for it.  Make that first
+ *          call during initialisation, before device memory is fixed and
+ *          before any stream capture.  The 32 MiB stay reserved until the
+ *          device's context ends; after a device reset the next call does
+ *          the set-up again.
+ *   Allocation: none on later calls (no cudaMalloc, cudaFree or allocating
  *          library routine).
- *   Set-up: the first call on a device (with that device current) looks up
- *          the array's device address with cudaGetSymbolAddress and keeps it;
- *          make that first call before any stream capture on the device.
  *   Sharing: every call on a device uses the same array, which keeps the
- *          last call's contents (nothing in it needs to start at zero).  Calls
- *          whose executions overlap on the GPU (other streams, other host
- *          threads) race on the array and give wrong results: serialise them.
+ *          last call's contents.  On a CSR that meets the contract nothing in
+ *          it needs to start at zero; on one that does not (see
+ *          csr_validate), or after USM_ERR_TIMEOUT, the output may hold values
+ *          left there by an earlier call.  Calls whose executions overlap on
+ *          the GPU (other streams, other host threads) race on the array and
+ *          give wrong results: serialise them.
  */
 int csr_sddmm_static_scratch(int M, int K, int D, int nnz,
                              const int *row_offsets, const int *col_indices,

@@ -68,12 +68,3 @@ def oracle_sddmm(csr, X, Y, dtype, rows=None):
     out = oracle.sddmm(M, csr.K, ro, ci, Xw, Yw)
     S = oracle.sddmm_error_scale(M, csr.K, ro, ci, Xw, Yw)
     return out, S, pos
-
-
-def sample_rows(M, n, seed, perm=None):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(M, size=min(n, M), replace=False).tolist())
-    rows.update([0, M - 1])
-    if perm is not None:  # the longest and the shortest rows too
-        rows.update([int(perm[0]), int(perm[-1])])
-    return np.array(sorted(rows), dtype=np.int64)

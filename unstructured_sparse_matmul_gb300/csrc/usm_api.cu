@@ -17,10 +17,22 @@ __device__ int g_status_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::atomic<int*> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
 std::once_flag g_encode_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_ctx_once;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+std::mutex g_symbol_mutex;
+
+void* driver_entry(const char* name, unsigned version) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return fn;
+    return nullptr;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -40,16 +52,39 @@ __global__ void wait_timeout_selftest_kernel(long long limit_ns, int* status) {
 
 }  // namespace
 
-int* status_word_for_current_device() {
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, [] {
+        g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(driver_entry("cuCtxGetCurrent", 4000));
+        g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(driver_entry("cuCtxGetId", 12000));
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+void* SymbolAddressCache::get() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    int* p = g_status_ptr[dev].load(std::memory_order_acquire);
-    if (p) return p;
+    std::lock_guard<std::mutex> lock(g_symbol_mutex);
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && ctx == ctx_[dev] && addr_[dev] != nullptr) return addr_[dev];
+    // First use in this context (or no context current yet): the lookup
+    // makes the device's primary context current and may load the module.
     void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
-    g_status_ptr[dev].store(static_cast<int*>(addr), std::memory_order_release);
-    return static_cast<int*>(addr);
+    if (cudaGetSymbolAddress(&addr, symbol_) != cudaSuccess || addr == nullptr) return nullptr;
+    ctx_[dev] = current_context_id();
+    addr_[dev] = addr;
+    return addr;
 }
+
+namespace {
+SymbolAddressCache g_status_cache(&g_status_word);
+}  // namespace
+
+int* status_word_for_current_device() { return static_cast<int*>(g_status_cache.get()); }
 
 int sm_count_current_device() {
     int dev = 0;
@@ -65,12 +100,7 @@ int sm_count_current_device() {
 bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool bf16, long long rows,
                           long long cols, long long ld_elems, int box_cols, int box_rows) {
     std::call_once(g_encode_once, [] {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(driver_entry("cuTensorMapEncodeTiled", 12000));
     });
     if (!g_encode) return false;
     const int es = bf16 ? 2 : 4;

@@ -11,6 +11,28 @@
 
 namespace usm {
 
+// Device address of a __device__ variable (`symbol`: its host-side name,
+// which is not a device address) in the calling thread's current context,
+// looked up with cudaGetSymbolAddress.  The lookup may load the module that
+// holds the variable.  The address is cached per device and per context:
+// after a device reset or a new primary context the next call looks it up
+// again.  Thread-safe.  nullptr if it cannot be resolved.
+class SymbolAddressCache {
+  public:
+    explicit SymbolAddressCache(const void* symbol) : symbol_(symbol) {}
+    void* get();
+
+  private:
+    static constexpr int kMaxDevices = 64;
+    const void* symbol_;
+    unsigned long long ctx_[kMaxDevices] = {};  // context id the address belongs to (0: none)
+    void* addr_[kMaxDevices] = {};
+};
+
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), or 0
+// when no context is current or the driver entry points are missing.
+unsigned long long current_context_id();
+
 // Device status word of the current device (null if it cannot be resolved).
 int* status_word_for_current_device();
 

@@ -371,14 +371,25 @@ __global__ void __launch_bounds__(W * 32, MINB)
     }
 }
 
-// out[p] = Σ_s partial[s][p] (strips added in increasing order), times the
-// mask's value when scaling.
+// Strips are added in increasing order in runs of kStripRun: the strips of
+// each run sequentially, then the run totals in order.  Up to kStripRun
+// strips this is one sequential sum; beyond, it keeps the additions along an
+// output's path to ≤ 63 + nstrips/64 (on top of ≤ 20 inside a strip), so the
+// fp32 worst-case rounding bound holds for D up to about 680k columns.
+constexpr int kStripRun = 64;
+
+// out[p] = Σ_s partial[s][p], times the mask's value when scaling.
 __global__ void sddmm_strip_sum_kernel(const float* __restrict__ part, long long nnz, int nstrips,
                                        void* out, int out_bf16, const void* scale, int scale_bf16) {
     for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < nnz;
          p += (long long)gridDim.x * blockDim.x) {
-        float s = part[p];
-        for (int k = 1; k < nstrips; ++k) s += part[(long long)k * nnz + p];
+        float s = 0.f;
+        for (int k0 = 0; k0 < nstrips; k0 += kStripRun) {
+            float t = part[(long long)k0 * nnz + p];
+            const int k1 = min(nstrips, k0 + kStripRun);
+            for (int k = k0 + 1; k < k1; ++k) t += part[(long long)k * nnz + p];
+            s = k0 == 0 ? t : s + t;
+        }
         if (scale) s *= scale_at(scale, scale_bf16, p);
         if (out_bf16)
             reinterpret_cast<uint16_t*>(out)[p] = f32_to_bf16_rne(s);
@@ -394,14 +405,26 @@ __global__ void sddmm_strip_sum4_kernel(const float4* __restrict__ part, long lo
                                         int out_bf16, const void* scale, int scale_bf16) {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
          i += (long long)gridDim.x * blockDim.x) {
-        float4 s = __ldcs(part + i);
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k0 = 0; k0 < nstrips; k0 += kStripRun) {
+            float4 t = __ldcs(part + (long long)k0 * n4 + i);
+            const int k1 = min(nstrips, k0 + kStripRun);
 #pragma unroll 4
-        for (int k = 1; k < nstrips; ++k) {
-            const float4 v = __ldcs(part + (long long)k * n4 + i);
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+            for (int k = k0 + 1; k < k1; ++k) {
+                const float4 v = __ldcs(part + (long long)k * n4 + i);
+                t.x += v.x;
+                t.y += v.y;
+                t.z += v.z;
+                t.w += v.w;
+            }
+            if (k0 == 0) {
+                s = t;
+            } else {
+                s.x += t.x;
+                s.y += t.y;
+                s.z += t.z;
+                s.w += t.w;
+            }
         }
         if (scale) {
             if (scale_bf16) {

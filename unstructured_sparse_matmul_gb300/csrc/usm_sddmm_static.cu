@@ -9,13 +9,14 @@
 // entry point takes its scratch from one fixed array in the library's own
 // device image instead, so it allocates nothing on any call.
 //
-// The array below is sized kStaticScratchBytes (32 MiB).  Every GPU that
-// loads this library keeps those 32 MiB until the process exits.  In host
-// code the array's name is only a host-side stand-in for the symbol, never a
-// device address: the device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and passed to the kernels.
-#include <atomic>
-
+// The array below is sized kStaticScratchBytes (32 MiB).  It is reserved on a
+// device when this file's module is loaded there: CUDA loads modules lazily,
+// so that happens at the first call on the device (the address lookup
+// below), and the 32 MiB stay reserved until the context ends.  In host code
+// the array's name is only a host-side stand-in for the symbol, never a
+// device address: the device address is looked up with cudaGetSymbolAddress
+// (with that device current) and passed to the kernels; it is looked up again
+// after a device reset or in a new context.
 #include "usm_device.cuh"
 #include "usm_internal.h"
 
@@ -25,24 +26,7 @@ constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
 
 static __device__ __align__(256) float g_sddmm_static_scratch[kStaticScratchBytes / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-
-// Device address of the scratch array on the current device.  The first
-// call on a device resolves it; later calls reuse it.
-int scratch_for_current_device(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return USM_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return USM_ERR_UNSUPPORTED;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-        const cudaError_t err = cudaGetSymbolAddress(&p, g_sddmm_static_scratch);
-        if (err != cudaSuccess || p == nullptr) return USM_ERR_CUDA;
-        g_scratch_addr[dev].store(p, std::memory_order_release);
-    }
-    *out = p;
-    return USM_OK;
-}
+usm::SymbolAddressCache g_scratch_cache(&g_sddmm_static_scratch);
 
 }  // namespace
 
@@ -54,12 +38,12 @@ extern "C" int csr_sddmm_static_scratch(int M, int K, int D, int nnz, const int*
     if (need > kStaticScratchBytes) return USM_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     if (need > 0) {
-        const int st = scratch_for_current_device(&scratch);
-        if (st != USM_OK) return st;
+        scratch = g_scratch_cache.get();
+        if (scratch == nullptr) return USM_ERR_CUDA;
     }
-    // Every strip writes its partial for every nonzero before the strip sum
-    // reads it, so nothing left in the array by an earlier call is ever read:
-    // no clearing is needed.
+    // On a valid CSR every strip writes its partial for every nonzero before
+    // the strip sum reads it, so nothing an earlier call left in the array is
+    // read and nothing needs clearing.
     return csr_sddmm(M, K, D, nnz, row_offsets, col_indices, row_swizzle, seg_rows, X, ldx, Y, ldy, out, in_dtype,
                      out_dtype, scratch, need > 0 ? kStaticScratchBytes : 0, stream);
 }

@@ -8,12 +8,12 @@
 namespace usm {
 namespace {
 
-template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB>
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK = false>
 int launch_cfg(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaStream_t stream) {
     using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::BOX_COLS, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS, MB>;
+    auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK>;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -112,6 +112,13 @@ int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) 
     if (ov.rows_per_warp == RA) R = RA, T = ta;
     else if (ov.rows_per_warp == RB) R = RB, T = tb;
     else if (ov.rows_per_warp != 0) return USM_ERR_UNSUPPORTED;
+    // fp32 with more than 128 chunks of K: the kernel with a second-level
+    // accumulator keeps the worst-case rounding bound (RA rows a warp only,
+    // for the registers it takes).
+    if (!BF && (a.K + KC - 1) / KC > 128) {
+        if (ov.rows_per_warp == RB) return USM_ERR_UNSUPPORTED;
+        return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB, true>(a, ta, B, ldb, stream);
+    }
     if (R == RA) return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB>(a, T, B, ldb, stream);
     return launch_cfg<BF, L, VEC, RB, W, KC, NS, MB>(a, T, B, ldb, stream);
 }

@@ -40,9 +40,12 @@
 //   across groups at the end.
 // * Accuracy.  In fp32 each window of ≤ 32 nonzeros is summed into a fresh
 //   accumulator, windows are added into a per-(row, chunk) partial and those
-//   into the row total: with ≤ 32 + 7 + K/KC additions along any output's
-//   path the worst-case rounding bound stays below 1e-5·Σ|a||b| while
-//   K/KC ≤ 128 (K up to 12288 with KC = 96).
+//   into the row total: ≤ 32 + KC/32 + 1 + K/KC additions lie along any
+//   output's path, which keeps the worst-case rounding bound (about one unit
+//   roundoff, 2^-24, per addition) below 1e-5·Σ|a||b| while K/KC ≤ 128.
+//   Longer K (LONGK) adds one more level: every 64 chunks the row total is
+//   moved into a second accumulator, so the path is ≤ 32 + KC/32 + 1 + 64 +
+//   K/(64·KC) additions (the bound holds to K ≈ 786k with KC = 192).
 #pragma once
 
 #include <climits>
@@ -120,7 +123,7 @@ __device__ __forceinline__ void load_window(const SpmmArgs& a, int pos, int end,
     }
 }
 
-template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB>
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK = false>
 __global__ void __launch_bounds__(W * 32, MB)
     spmm_kernel(const __grid_constant__ CUtensorMap tmB, const SpmmArgs a) {
     using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
@@ -219,10 +222,17 @@ __global__ void __launch_bounds__(W * 32, MB)
     }
 
     float acc[R][VEC];
+    float acc_hi[LONGK ? R : 1][LONGK ? VEC : 1];  // LONGK: totals of whole 64-chunk runs
 #pragma unroll
     for (int i = 0; i < R; ++i)
 #pragma unroll
         for (int v = 0; v < VEC; ++v) acc[i][v] = 0.f;
+    if constexpr (LONGK) {
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc_hi[i][v] = 0.f;
+    }
 
     int cur = my_start;  // lane i: cursor of row slot i
     // PERSIST (one CTA per SM, registers to spare): each row slot keeps a
@@ -423,6 +433,17 @@ __global__ void __launch_bounds__(W * 32, MB)
                 }
             }
         }
+        if constexpr (LONGK) {
+            if ((j & 63) == 63) {
+#pragma unroll
+                for (int i = 0; i < R; ++i)
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) {
+                        acc_hi[i][v] += acc[i][v];
+                        acc[i][v] = 0.f;
+                    }
+            }
+        }
         __syncthreads();  // every warp is done with stage s
         if (kr[2]) break;
         if (threadIdx.x == 0 && j + NS < nchunks) {
@@ -451,7 +472,7 @@ __global__ void __launch_bounds__(W * 32, MB)
     for (int i = 0; i < R; ++i)
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-            float x = acc[i][v];
+            float x = LONGK ? acc_hi[i][v] + acc[i][v] : acc[i][v];
             if (G >= 2) x += __shfl_xor_sync(kFullMask, x, L);
             if (G >= 4) x += __shfl_xor_sync(kFullMask, x, 2 * L);
             if (G >= 8) x += __shfl_xor_sync(kFullMask, x, 4 * L);

@@ -71,7 +71,8 @@ __global__ void permute_kernel(int nnz, const int* __restrict__ perm, const T* _
 
 int grid_for(long long n) {
     long long b = (n + 255) / 256;
-    if (b > 8 * 152) b = 8 * 152;
+    const long long cap = 8LL * sm_count_current_device();
+    if (b > cap) b = cap;
     return (int)(b < 1 ? 1 : b);
 }
 
