@@ -36,10 +36,10 @@ FP32_LANES_PER_SM = 128
 SM_MAX_MHZ_DEFAULT = 2070.0  # GB300's maximum SM clock, when nothing better is known
 # On-chip operand delivery: every useful FMA reads one dense-operand element
 # from shared memory that no other FMA of its lane reuses, and shared memory
-# delivers 125 B/clk/SM to 128-bit loads at random staged rows (measured on
-# GB300: profiles/operand_bound.md): at most 125/4 fp32 (125/2 bf16) FMAs per
-# clock per SM.
-SMEM_BYTES_PER_CLK = 125.0
+# delivers 128 B/clk/SM to 32-, 64- and 128-bit loads at random staged rows
+# (measured on GB300 with clock64() in every CTA: profiles/operand_bound.md):
+# at most 128/4 fp32 (128/2 bf16) FMAs per clock per SM.
+SMEM_BYTES_PER_CLK = 128.0
 
 
 class Device:
@@ -87,7 +87,10 @@ WORKLOADS = {
     "ffn": "the hot path: SpMM forward + SDDMM weight-gradient per FFN problem (the bench line)",
     "ffn_train": "the sparse layer's training step per FFN problem: forward SpMM, weight-gradient SDDMM "
                  "(X = dC, Y = B), weights permuted into Aᵀ order, input-gradient SpMM on Aᵀ",
-    "attention": "sparse attention, 8 heads x 4096, bf16: SDDMM scores, row softmax, SpMM with V",
+    "attention": "sparse attention, 8 heads x 4096, bf16: SDDMM scores, then the SpMM with V with the row softmax "
+                 "fused into it (csr_spmm_row_softmax)",
+    "attention_unfused": "sparse attention, 8 heads x 4096, bf16: SDDMM scores, row softmax to bf16, SpMM with V "
+                         "(three calls)",
     "lstm": "LSTM-sized sweep, fp32: A 8192x4096 at 50/60/70/80/90/95/98%, B 4096x128, SpMM only",
     "resnet": "ResNet-50-like 1x1 conv, fp32: A 512x2048 at 80%, B 2048x3136 SpMM and SDDMM weight-gradient "
               "(X 512x3136, Y 2048x3136); L2 flushed before every step",
@@ -104,7 +107,7 @@ FLUSH_L2 = {"resnet"}
 def problems(only=None, workload="ffn"):
     """Problems of one step.  `only` keeps the problems whose tag contains
     that substring."""
-    if workload == "attention":
+    if workload.startswith("attention"):
         return [W.attention()]
     keep = lambda p: not only or only.split(":")[-1] in tag_of(p.dtype, p.csr.M, p.csr.K, p.meta["sparsity"])
     if workload == "lstm":
@@ -131,6 +134,8 @@ def ops_of(only, workload="ffn"):
     if workload == "ffn_train":
         return ("spmm", "sddmm_w", "permute", "spmm_t")
     if workload == "attention":
+        return ("sddmm", "spmm_softmax")
+    if workload == "attention_unfused":
         return ("sddmm", "softmax", "spmm")
     if workload == "lstm":
         return ("spmm",)
@@ -155,6 +160,8 @@ def alg_bytes(p, op):
     M, K, nnz, N = p.csr.M, p.csr.K, p.csr.nnz, width_of(p)
     if op == "spmm":
         return nnz * (es + 4) + 4 * (M + 1) + K * N * es + 4 * M * N
+    if op == "spmm_softmax":  # fp32 scores as values
+        return nnz * (4 + 4) + 4 * (M + 1) + K * N * es + 4 * M * N
     if op == "spmm_t":  # Aᵀ (K x M) · dC (M x N) -> K x N
         return nnz * (es + 4) + 4 * (K + 1) + M * N * es + 4 * K * N
     if op == "permute":
@@ -262,10 +269,10 @@ def run_ours(args, rank, world, local_rank):
         N = width_of(p)
         bf = p.dtype == "bf16"
         d = {"p": p, "ro": to_dev(csr.row_offsets, "i32"), "ci": to_dev(csr.col_indices, "i32")}
-        seg = p.meta.get("seq", 0) if wl == "attention" else 0
+        seg = p.meta.get("seq", 0) if wl.startswith("attention") else 0
         d["perm"] = usm.row_swizzle(d["ro"], csr.K, seg_rows=seg)
         d["seg"] = seg
-        if wl == "attention":
+        if wl.startswith("attention"):
             d["X"], d["Y"], d["V"] = to_dev(p.X, "bf16"), to_dev(p.Y, "bf16"), to_dev(p.V, "bf16")
             d["S"] = torch.empty(csr.nnz, dtype=torch.float32, device=dev)
             d["P"] = torch.empty(csr.nnz, dtype=torch.bfloat16, device=dev)
@@ -307,17 +314,20 @@ def run_ours(args, rank, world, local_rank):
     launches = []
     for d in items:
         p = d["p"]
-        tag = "bf16_8x4096_h64" if wl == "attention" else tag_of(p.dtype, p.csr.M, p.csr.K, p.meta["sparsity"])
+        tag = "bf16_8x4096_h64" if wl.startswith("attention") else tag_of(p.dtype, p.csr.M, p.csr.K, p.meta["sparsity"])
         for op in ops_of(args.only, wl):
             launches.append((f"{op}_{tag}", op, d))
     kernels_per_launch = {label: (d["nk_sddmm"] if op.startswith("sddmm") else 1) for label, op, d in launches}
 
     def run_one(op, d):
         K = d["p"].csr.K
-        if wl == "attention":
+        if wl.startswith("attention"):
             seg = d["p"].meta["seq"]
             if op == "sddmm":
                 usm.sddmm(d["ro"], d["ci"], d["X"], d["Y"], row_swizzle=d["perm"], out=d["S"], seg_rows=seg)
+            elif op == "spmm_softmax":
+                usm.spmm_row_softmax(d["ro"], d["ci"], d["S"], d["V"], K=K, row_swizzle=d["perm"], out=d["C"],
+                                     seg_rows=seg)
             elif op == "softmax":
                 usm.row_softmax(d["ro"], d["S"], out=d["P"])
             else:
@@ -511,7 +521,7 @@ def run_ours(args, rank, world, local_rank):
                                     f"{Device.sm_max_mhz / 1e3:.3g} GHz",
                      "operand_bound": {"peak": round(operand_bound_tflops(2 if "bf16" in dom_label else 4), 2),
                                        "frac": dom["frac_operand_bound"],
-                                       "source": "shared-memory delivery 125 B/clk/SM (profiles/operand_bound.md), "
+                                       "source": "shared-memory delivery 128 B/clk/SM (profiles/operand_bound.md), "
                                                  "one dense element per useful FMA"}},
         "setup": {"row_swizzle_ms_all_patterns": round(swz_ms, 4), "patterns": len(items)},
         # Measured character of every generated matrix (sparsity within its

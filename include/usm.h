@@ -220,11 +220,42 @@ int csr_sddmm_general(int M, int K, int D, int nnz,
  * scores fp32 [nnz], out fp32 or bf16 (nearest even) [nnz]; empty rows write
  * nothing.  The normalisation step between the SDDMM scores and the SpMM of
  * sparse attention (the sparse-attention use of the kernels, "Interesting
- * ideas" I3).  Rounding: ≤ n/32 + 8 fp32 roundings per output for a row of n
- * entries (lane sums, a 5-level tree, exp and one division).
+ * ideas" I3).  Error: ≤ n/128 + 9 fp32 roundings per output for a row of n
+ * entries (four partial sums a lane, a 2-level and a 5-level tree, a
+ * reciprocal of the sum and one product) on top of the exponentials', which
+ * use the fast hardware exp (CUDA's __expf: at most 2 + 1.17·|s - m| ulp).
+ * csr_spmm_row_softmax forms the same values bit for bit.
  */
 int csr_row_softmax(int M, int nnz, const int *row_offsets, const float *scores, void *out,
                     usm_dtype out_dtype, void *stream);
+
+/*
+ * csr_spmm_row_softmax — sparse attention's softmax fused into the SpMM:
+ *   C[r][j] = Σ_{p in row r} P[p] · B[col_indices[p]][j],
+ *   P[p] = exp(s[p] - m_r) / Σ_{q in row r} exp(s[q] - m_r),  m_r = max_{q in row r} s[q],
+ * the row softmax over each row's stored entries of the fp32 `scores` (the
+ * SDDMM output of the sparse-attention chain), taken inside the product.
+ * Each P[p] is formed in fp32 exactly as csr_row_softmax forms it (same
+ * operations in the same order, bit for bit), then rounded to `dtype`
+ * (USM_BF16: nearest even; USM_F32: unchanged) and multiplied as csr_spmm
+ * multiplies values: the result is bit-identical to csr_row_softmax into a
+ * `dtype` buffer followed by csr_spmm on it, without that buffer's write and
+ * read.  Source: "Sparse GPU Kernels for Deep Learning", summary card,
+ * "Interesting ideas" I3 (the SDDMM and SpMM of sparse attention); the
+ * softmax between them is this library's.
+ *
+ *   scores : fp32 [nnz] in the CSR order of (row_offsets, col_indices).
+ *   B      : K×N dense, row-major, ldb ≥ N, elements of `dtype`.
+ *   C      : M×N fp32, ldc ≥ N, overwritten; empty rows give zero rows.
+ *   row_swizzle, seg_rows : as csr_spmm (schedule only).
+ * Limits, alignment and empty cases as csr_spmm.
+ */
+int csr_spmm_row_softmax(int M, int K, int N, int nnz,
+                         const int *row_offsets, const int *col_indices, const float *scores,
+                         const int *row_swizzle, int seg_rows,
+                         const void *B, int ldb,
+                         float *C, int ldc,
+                         usm_dtype dtype, void *stream);
 
 /*
  * csr_transpose — Aᵀ in CSR, for the sparse layer's input gradient.

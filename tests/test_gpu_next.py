@@ -168,12 +168,65 @@ def test_row_softmax(usm):
     ro = dev(csr.row_offsets)
     p32 = host(usm.row_softmax(ro, dev(s)))
     ref = oracle.csr_softmax(csr.row_offsets, s.astype(np.float64))
-    # ≤ n/32 + 8 roundings per output with n ≤ 5000: 165 u < 1e-5 relative
-    assert np.all(np.abs(p32 - ref) <= 1e-5 * ref)
+    # ≤ n/128 + 9 roundings per output with n ≤ 5000 (≤ 49 u) plus the fast
+    # exponential's ≤ 2 + 1.17·|s - m| ulp (|s - m| < 25 here: ≤ 32 u):
+    # under 100 u = 6e-6 relative, checked against 2e-5
+    assert np.all(np.abs(p32 - ref) <= 2e-5 * ref)
     p16 = host(usm.row_softmax(ro, dev(s), out_dtype=torch.bfloat16))
     want = oracle.round_to_bf16(ref)
     assert np.all(np.abs(p16.astype(np.int64) - want.astype(np.int64)) <= 1)
     assert np.mean(p16 == want) > 0.99
+
+
+FUSED_CASES = [(64, 0.05, 0), (128, 0.1, 0), (300, 0.2, 0), (64, 0.3, 250)]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N,density,seg", FUSED_CASES)
+@pytest.mark.parametrize("swz", [False, True])
+def test_spmm_row_softmax_matches_unfused_chain(usm, dtype, N, density, seg, swz):
+    """The fused softmax-SpMM gives the bits of csr_row_softmax into a
+    buffer of B's type followed by csr_spmm, and the oracle chain's result
+    within tolerance (empty, single-entry and long rows included)."""
+    import torch
+    M, K = 1000, 1500
+    rng = np.random.default_rng([N, seg, 21])
+    lengths = rng.binomial(K, density, M)
+    lengths[:10] = 0
+    lengths[10:20] = 1
+    lengths[20] = K
+    if seg:  # block-diagonal rows: each block of seg rows only touches its own columns
+        K = M
+        lengths = np.minimum(lengths, seg)
+        base = (np.arange(M) // seg) * seg
+        ro, ci = W.csr_from_lengths(rng, lengths, seg, col_base=base)
+        csr = W.CSR(M, K, ro, ci, W.values_for(rng, int(ro[-1]), 1.0, dtype), dtype, seg_rows=seg)
+    else:
+        csr = W.random_csr([N, 22], M, K, 0.0, dtype=dtype, lengths=lengths)
+    s = (rng.standard_normal(csr.nnz) * 3).astype(np.float32)
+    B = W.dense(rng, K, N, 1.0, dtype)
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    perm = usm.row_swizzle(ro, K, seg) if swz else None
+    Bd, sd = dev(B, dtype), dev(s)
+    fused = host(usm.spmm_row_softmax(ro, ci, sd, Bd, K=K, row_swizzle=perm, seg_rows=seg))
+    P = usm.row_softmax(ro, sd, out_dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
+    unfused = host(usm.spmm(ro, ci, P, Bd, K=K, row_swizzle=perm, seg_rows=seg))
+    assert np.array_equal(fused, unfused)
+    assert usm.poll_status() == 0
+    # the oracle chain: fp64 softmax (rounded to bf16 for bf16), fp64 SpMM
+    p64 = oracle.csr_softmax(csr.row_offsets, s.astype(np.float64))
+    if dtype == "bf16":
+        p64 = oracle.widen(oracle.round_to_bf16(p64), "bf16")
+    Bw = oracle.widen(B, dtype)
+    ref = oracle.spmm(M, K, csr.row_offsets, csr.col_indices, p64, Bw)
+    S = oracle.spmm_error_scale(M, K, csr.row_offsets, csr.col_indices, p64, Bw)
+    # fp32: the probabilities carry <= n/128 + 9 roundings and the fast
+    # exponential's <= 2 + 1.17·|s - m| ulp (under 100 u = 6e-6 relative for
+    # n <= 1500, |s - m| < 25) on top of the SpMM's 1e-5; bf16: one bf16 ulp
+    # (2^-7 relative) between the GPU's rounding of its fp32 probability and
+    # the oracle's rounding of the exact one
+    tol = 2e-5 if dtype == "f32" else TOL["bf16"] + 2.0 ** -7
+    assert_within(fused, ref, S, tol, f"fused softmax spmm {dtype} N={N}")
 
 
 @pytest.mark.slow
@@ -206,6 +259,33 @@ def test_attention_chain_with_softmax(usm):
     ref = oracle.spmm(csr.M, csr.K, ro_h, ci_h, w64, Vw)
     S = oracle.spmm_error_scale(csr.M, csr.K, ro_h, ci_h, w64, Vw)
     assert_within(O, ref, S, TOL["bf16"] + 2.0 ** -7, "attention with softmax vs the oracle chain")
+
+
+@pytest.mark.slow
+def test_attention_chain_fused_softmax(usm):
+    """The attention chain with the softmax inside the SpMM: SDDMM scores
+    (fp32), then csr_spmm_row_softmax with V.  Every output element equals
+    the unfused chain's (csr_row_softmax to bf16, then csr_spmm) bit for bit
+    and the oracle chain's within tolerance."""
+    import torch
+    p = W.attention()
+    csr = p.csr
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    seg = p.meta["seq"]
+    perm = usm.row_swizzle(ro, csr.K, seg_rows=seg)
+    V = dev(p.V, "bf16")
+    scores = usm.sddmm(ro, ci, dev(p.X, "bf16"), dev(p.Y, "bf16"), row_swizzle=perm, seg_rows=seg)
+    O = host(usm.spmm_row_softmax(ro, ci, scores, V, K=csr.K, row_swizzle=perm, seg_rows=seg))
+    probs = usm.row_softmax(ro, scores, out_dtype=torch.bfloat16)
+    O_unfused = host(usm.spmm(ro, ci, probs, V, K=csr.K, row_swizzle=perm, seg_rows=seg))
+    assert np.array_equal(O, O_unfused)
+    ro_h, ci_h = csr.row_offsets, csr.col_indices
+    s64 = oracle.sddmm(csr.M, csr.K, ro_h, ci_h, oracle.widen(p.X, "bf16"), oracle.widen(p.Y, "bf16"))
+    w64 = oracle.widen(oracle.round_to_bf16(oracle.csr_softmax(ro_h, s64)), "bf16")
+    Vw = oracle.widen(p.V, "bf16")
+    ref = oracle.spmm(csr.M, csr.K, ro_h, ci_h, w64, Vw)
+    S = oracle.spmm_error_scale(csr.M, csr.K, ro_h, ci_h, w64, Vw)
+    assert_within(O, ref, S, TOL["bf16"] + 2.0 ** -7, "fused attention vs the oracle chain")
 
 
 # ---------------------------------------------------------------------------

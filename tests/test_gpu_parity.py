@@ -345,13 +345,15 @@ def test_attention_chain(usm):
     # scores, every nonzero of the 32768-row stack
     ref_s, S_s, _ = oracle_sddmm(csr, p.X, p.Y, "bf16")
     assert_within(host(s32), ref_s, S_s, TOL["bf16"], "attention scores")
-    # rounded scores: bf16 of the fp32 sums; equal to the oracle's rounding
-    # except where the fp32 sum and the exact sum straddle a rounding tie
-    # (the GPU rounds its fp32 sum, the oracle its fp64 sum: one ulp apart at most)
+    # rounded scores: each is its fp32 score rounded to nearest even, bit for
+    # bit (rounded here by the oracle's rounding of the widened fp32 value);
+    # against the oracle's own rounding of the exact scores they agree except
+    # where the fp32 sum and the exact sum fall on two sides of a rounding
+    # boundary, or straddle zero in a cancelling sum
     got16 = host(s16)
+    assert np.array_equal(got16, oracle.round_to_bf16(host(s32).astype(np.float64)))
     want16 = oracle.round_to_bf16(ref_s)
-    diff = np.abs(got16.astype(np.int64) - want16.astype(np.int64))
-    assert np.all(diff <= 1) and np.mean(diff == 0) > 0.99
+    assert np.mean(got16 == want16) > 0.99
     # chain output, every element: the SpMM against the oracle on the GPU's
     # own rounded scores (its actual inputs) ...
     Vw = oracle.widen(p.V, "bf16")

@@ -46,6 +46,7 @@ SIGNATURES = {
     "csr_transpose": (_i, [_i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "csr_permute_values": (_i, [_i, _vp, _vp, _i, _vp, _vp]),
     "csr_validate": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp]),
+    "csr_spmm_row_softmax": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _vp]),
 }
 
 # csr_validate result codes (usm_csr_check in include/usm.h).
@@ -199,6 +200,30 @@ def spmm(row_offsets, col_indices, values, B, K: int | None = None, row_swizzle=
                         _ptr(row_swizzle), seg_rows, _ptr(B), _ld(B), _ptr(C), _ld(C), _dtype_code(values),
                         _stream(stream))
     _check("csr_spmm", code)
+    return C
+
+
+def spmm_row_softmax(row_offsets, col_indices, scores, B, K: int | None = None, row_swizzle=None, out=None,
+                     stream=None, seg_rows: int = 0):
+    """C = softmax_rows(scores)·B (fp32 out): each row's stored fp32 scores
+    turned into softmax probabilities, rounded to B's element type (fp32 or
+    bf16), inside the product; see csr_spmm_row_softmax."""
+    torch = _torch()
+    lib = load()
+    _require(row_offsets, "row_offsets", (torch.int32,))
+    _require(col_indices, "col_indices", (torch.int32,))
+    _require(scores, "scores", (torch.float32,))
+    _require(B, "B", (torch.float32, torch.bfloat16))
+    M = row_offsets.numel() - 1
+    K = B.shape[0] if K is None else K
+    N = B.shape[1]
+    B = _tma_ready(B)
+    C = out if out is not None else _new_dense_out(M, N, B.device)
+    _require(C, "out", (torch.float32,))
+    code = lib.csr_spmm_row_softmax(M, K, N, col_indices.numel(), _ptr(row_offsets), _ptr(col_indices), _ptr(scores),
+                                    _ptr(row_swizzle), seg_rows, _ptr(B), _ld(B), _ptr(C), _ld(C), _dtype_code(B),
+                                    _stream(stream))
+    _check("csr_spmm_row_softmax", code)
     return C
 
 

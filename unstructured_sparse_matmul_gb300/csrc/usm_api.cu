@@ -160,6 +160,29 @@ int csr_spmm(int M, int K, int N, int nnz, const int* row_offsets, const int* co
     return launch_spmm(a, B, ldb, dtype == USM_BF16, st);
 }
 
+int csr_spmm_row_softmax(int M, int K, int N, int nnz, const int* row_offsets, const int* col_indices,
+                         const float* scores, const int* row_swizzle, int seg_rows, const void* B, int ldb, float* C,
+                         int ldc, usm_dtype dtype, void* stream) {
+    if (M < 0 || K < 0 || N < 0 || nnz < 0) return USM_ERR_INVALID_ARG;
+    if (dtype != USM_F32 && dtype != USM_BF16) return USM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return USM_OK;
+    if (ldc < N) return USM_ERR_INVALID_ARG;
+    if (!C || !row_offsets) return USM_ERR_INVALID_ARG;
+    if (!aligned16(C) || (ldc % 4) != 0) return USM_ERR_ALIGNMENT;
+    if (nnz > 0 && K == 0) return USM_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    if (nnz == 0) return launch_fill_f32(C, M, N, ldc, st);
+    if (!col_indices || !scores || !B) return USM_ERR_INVALID_ARG;
+    if (ldb < N) return USM_ERR_INVALID_ARG;
+    const int es = dtype == USM_BF16 ? 2 : 4;
+    if (!aligned16(B) || ((long long)ldb * es) % 16 != 0) return USM_ERR_ALIGNMENT;
+    int* status = status_word_for_current_device();
+    if (!status) return USM_ERR_CUDA;
+    SpmmArgs a{M, K, N, nnz, row_offsets, col_indices, scores, row_swizzle, effective_seg(M, seg_rows), C, ldc,
+               status};
+    return launch_spmm(a, B, ldb, dtype == USM_BF16, st, true);
+}
+
 size_t csr_sddmm_workspace_bytes(int M, int K, int D, int nnz, usm_dtype in_dtype) {
     if (M <= 0 || K < 0 || D <= 0 || nnz <= 0) return 0;
     return sddmm_workspace_bytes(M, K, D, nnz, in_dtype == USM_BF16);

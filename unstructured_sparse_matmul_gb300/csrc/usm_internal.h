@@ -45,7 +45,9 @@ int sm_count_current_device();
 bool encode_tensor_map_2d(CUtensorMap* map, const void* base, bool bf16, long long rows,
                           long long cols, long long ld_elems, int box_cols, int box_rows);
 
-int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream);
+// softmax: a.values are fp32 scores and each row's values are their softmax
+// probabilities, rounded to B's element type (csr_spmm_row_softmax).
+int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream, bool softmax = false);
 int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream);
 
 size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16);

@@ -4,9 +4,8 @@
 // "Interesting ideas" I3):
 //     out[p] = exp(s[p] - m_r) / Σ_{q in row r} exp(s[q] - m_r),  m_r = max s.
 // One warp per row, three passes over the row (max, sum, write) so no
-// running rescale adds error: each lane sums its ~n/32 terms, then a
-// 5-level tree, then one division — about n/32 + 8 roundings along any path.
-#include <cfloat>
+// running rescale adds error (row_softmax_stats, softmax_prob: the same
+// routines the SpMM with a fused softmax uses, so the two agree bit for bit).
 
 #include "usm_device.cuh"
 #include "usm_internal.h"
@@ -23,16 +22,10 @@ __global__ void row_softmax_kernel(int M, int nnz, const int* __restrict__ ro, c
         b = min(max(b, 0), nnz);
         e = min(max(e, b), nnz);
         if (b == e) continue;
-        float m = -FLT_MAX;
-        for (int p = b + lane; p < e; p += 32) m = fmaxf(m, __ldg(s + p));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
-        float z = 0.f;
-        for (int p = b + lane; p < e; p += 32) z += expf(__ldg(s + p) - m);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFullMask, z, o);
+        float m, rz;
+        row_softmax_stats(s, b, e, lane, m, rz);
         for (int p = b + lane; p < e; p += 32) {
-            const float v = expf(__ldg(s + p) - m) / z;
+            const float v = softmax_prob(__ldg(s + p), m, rz);
             if (out_bf16)
                 reinterpret_cast<uint16_t*>(out)[p] = f32_to_bf16_rne(v);
             else

@@ -8,12 +8,19 @@
 namespace usm {
 namespace {
 
-template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK = false>
-int launch_cfg(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaStream_t stream) {
-    using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
+// 128-entry windows read with 16-byte loads (VL) against 32-entry windows
+// read one element a lane: USM_SPMM_VL=1 takes VL wherever the kernel
+// allows it (one lane group, no tensor-memory rows, aligned CSR arrays).
+#ifndef USM_SPMM_VL
+#define USM_SPMM_VL 0
+#endif
+
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK, bool TM, bool SMX, bool VL>
+int launch_kernel(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaStream_t stream) {
+    using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS, TM, VL>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::BOX_COLS, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK>;
+    auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK, TM, SMX, VL>;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -34,6 +41,17 @@ int launch_cfg(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaStre
     if (grid.y > 65535u) return USM_ERR_UNSUPPORTED;
     kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);
     return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
+}
+
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK = false, bool TM = false,
+          bool SMX = false>
+int launch_cfg(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaStream_t stream) {
+    if constexpr (USM_SPMM_VL && L == 32 && !TM) {
+        const bool aligned = (reinterpret_cast<uintptr_t>(a.col_indices) & 15u) == 0 &&
+                             (reinterpret_cast<uintptr_t>(a.values) & (BF ? 7u : 15u)) == 0;
+        if (aligned) return launch_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK, TM, SMX, true>(a, tiles_per_block, B, ldb, stream);
+    }
+    return launch_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK, TM, SMX, false>(a, tiles_per_block, B, ldb, stream);
 }
 
 }  // namespace
@@ -75,7 +93,8 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 //    shared-memory bandwidth is about five times what L2 delivers to TMA).
 // Measured against the fewest tiles: FFN SpMM 7-14% faster, LSTM 5-13%,
 // ResNet 31%, attention 6%.
-template <bool BF, int L, int VEC, int W, int KC, int NS, int MB, int RA = 2, int RB = 4>
+template <bool BF, int L, int VEC, int W, int KC, int NS, int MB, int RA = 2, int RB = 4, bool TM = false,
+          bool SMX = false>
 int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
     const int sms = sm_count_current_device();
     const long long slots = (long long)sms * MB;
@@ -117,24 +136,48 @@ int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) 
     // for the registers it takes).
     if (!BF && (a.K + KC - 1) / KC > 128) {
         if (ov.rows_per_warp == RB) return USM_ERR_UNSUPPORTED;
-        return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB, true>(a, ta, B, ldb, stream);
+        return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB, true, TM, SMX>(a, ta, B, ldb, stream);
     }
-    if (R == RA) return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB>(a, T, B, ldb, stream);
-    return launch_cfg<BF, L, VEC, RB, W, KC, NS, MB>(a, T, B, ldb, stream);
+    if (R == RA) return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB, false, TM, SMX>(a, T, B, ldb, stream);
+    return launch_cfg<BF, L, VEC, RB, W, KC, NS, MB, false, TM, SMX>(a, T, B, ldb, stream);
 }
 
-int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
+// The six tile shapes by element type and N.  SMX: the values are the rows'
+// softmax probabilities of fp32 scores (csr_spmm_row_softmax).
+template <bool SMX>
+int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
     if (!bf16) {
-        if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1>(a, B, ldb, stream);
-        if (a.N <= 128) return launch_pick<false, 32, 4, W, 192 * F, NS, 1>(a, B, ldb, stream);
-        return launch_pick<false, 32, 8, W, 96 * F, NS, 1>(a, B, ldb, stream);
+        if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
+        if (a.N <= 128) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
+#ifndef USM_SPMM_TMEM
+#define USM_SPMM_TMEM 1
+#endif
+#ifndef USM_TM_MIN_DENSITY_PCT
+#define USM_TM_MIN_DENSITY_PCT 25
+#endif
+#ifndef USM_TM_RB
+#define USM_TM_RB 4
+#endif
+        // fp32 256-wide strips of masks at least a quarter set: the last 64
+        // rows of every chunk also go to tensor memory (measured on the FFN
+        // launches at 70% sparsity: 5-9% faster; at 80% even; 10-20% slower at
+        // 90-95%, where the copies and their waits are not paid back).
+        const long long kspan = a.seg_rows < a.M ? min(a.K, a.seg_rows) : a.K;  // columns a row block spans
+        if (!SMX && USM_SPMM_TMEM && NS == 1 &&
+            100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * a.M * kspan)
+            return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
+        return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
     }
-    if (a.N <= 64) return launch_pick<true, 16, 4, W, 384 * F, NS, 2>(a, B, ldb, stream);
-    if (a.N <= 128) return launch_pick<true, 32, 4, W, 192 * F, NS, 2>(a, B, ldb, stream);
+    if (a.N <= 64) return launch_pick<true, 16, 4, W, 384 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
+    if (a.N <= 128) return launch_pick<true, 32, 4, W, 192 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
     // 16 bf16 a lane (512-column strips in two TMA boxes, fewer instructions
     // per FMA) measured no faster at 70% and 6-25% slower at 90-95%.
-    return launch_pick<true, 32, 8, W, 96 * F, NS, 2>(a, B, ldb, stream);
+    return launch_pick<true, 32, 8, W, 96 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
+}
+
+int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream, bool softmax) {
+    return softmax ? launch_shape<true>(a, B, ldb, bf16, stream) : launch_shape<false>(a, B, ldb, bf16, stream);
 }
 
 }  // namespace usm

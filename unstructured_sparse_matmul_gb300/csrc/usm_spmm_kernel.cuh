@@ -51,13 +51,19 @@
 #include <climits>
 #include <type_traits>
 
+// Tensor-memory reads in software-pipelined pairs (1) or batches of four
+// behind one wait (0, measured faster: the pairs need more registers).
+#ifndef USM_TM_PIPE
+#define USM_TM_PIPE 0
+#endif
+
 #include "usm_device.cuh"
 #include "usm_args.h"
 
 namespace usm {
 namespace {
 
-template <bool BF, int L, int VEC, int R, int W, int KC, int NS>
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, bool TM = false, bool VL = false>
 struct SpmmCfg {
     static constexpr int ES = BF ? 2 : 4;          // element bytes
     static constexpr int NT = L * VEC;             // output columns per CTA (VEC per lane)
@@ -81,7 +87,10 @@ struct SpmmCfg {
     // value load of the split form cost more than its saved arithmetic there).
     static constexpr bool ADDR = BF && NCH == 0;
     static constexpr int ENTRY = ADDR ? 6 : (BF ? 4 : 8);
-    static constexpr int LIST_BYTES = W * 32 * ENTRY;
+    // A warp's list: 32 slots (one window); TM adds 32 for tensor-memory
+    // entries; VL windows hold 128 entries.
+    static constexpr int LIST_SLOTS = VL ? 128 : (TM ? 64 : 32);
+    static constexpr int LIST_BYTES = W * LIST_SLOTS * ENTRY;
     static constexpr int SMEM = NS * STAGE + 64 + LIST_BYTES;
     static_assert(NS == 1 || NS == 2, "one or two stages");
     static_assert(32 % L == 0, "L must divide the warp");
@@ -106,35 +115,106 @@ __device__ __forceinline__ int lane_col(int l, int v) {
 }
 
 // Window of 32 consecutive nonzeros of a row starting at `pos`: lane i gets
-// nonzero pos+i (column INT_MAX past the row end).
-template <bool BF>
+// nonzero pos+i (column INT_MAX past the row end).  SMX: val holds the raw
+// fp32 score; value_bits turns it into the probability when the entry is
+// listed (so the load's latency stays hidden behind other work).
+template <bool BF, bool SMX = false>
 __device__ __forceinline__ void load_window(const SpmmArgs& a, int pos, int end, int lane, int& col,
                                             uint32_t& val) {
     const int p = pos + lane;
     if (p < end) {
         col = __ldg(a.col_indices + p);
-        if (BF)
-            val = __ldg(reinterpret_cast<const unsigned short*>(a.values) + p);
-        else
+        if constexpr (SMX) {
             val = __ldg(reinterpret_cast<const unsigned int*>(a.values) + p);
+        } else if (BF) {
+            val = __ldg(reinterpret_cast<const unsigned short*>(a.values) + p);
+        } else {
+            val = __ldg(reinterpret_cast<const unsigned int*>(a.values) + p);
+        }
     } else {
         col = INT_MAX;
         val = 0;
     }
 }
 
-template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK = false>
+// The value bits a list entry carries: the stored value, or (SMX) the row's
+// softmax probability of the score (maximum m, reciprocal sum rz) rounded to
+// B's element type.
+template <bool BF, bool SMX>
+__device__ __forceinline__ uint32_t value_bits(uint32_t val, float m, float rz) {
+    if constexpr (SMX) {
+        const float v = softmax_prob(__uint_as_float(val), m, rz);
+        return BF ? (uint32_t)f32_to_bf16_rne(v) : __float_as_uint(v);
+    }
+    return val;
+}
+
+// VL: window of 128 consecutive nonzeros starting at `base` (a multiple of
+// 4, at or before the row cursor): lane i gets nonzeros base+4i..base+4i+3
+// with one 16-byte load of column indices and one 16-byte (fp32) or 8-byte
+// (bf16) load of values, when all four lie before the row end; else the ones
+// that do, one by one (column INT_MAX past the row end).  The entries before
+// the cursor (the misaligned start's residue) are loaded but never used:
+// the caller masks them by position.  Needs col_indices 16-byte aligned and
+// values 16-byte (fp32) or 8-byte (bf16) aligned; base >= 0 keeps every
+// load inside the arrays.
+template <bool BF, bool SMX = false>
+__device__ __forceinline__ void load_window_v(const SpmmArgs& a, int base, int end, int lane, int (&col)[4],
+                                              uint32_t (&val)[4]) {
+    const int p = base + 4 * lane;
+    if (!SMX && p + 4 <= end) {
+        const int4 c = __ldg(reinterpret_cast<const int4*>(a.col_indices + p));
+        col[0] = c.x;
+        col[1] = c.y;
+        col[2] = c.z;
+        col[3] = c.w;
+        if constexpr (BF) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(a.values) + p));
+            val[0] = v.x & 0xffffu;
+            val[1] = v.x >> 16;
+            val[2] = v.y & 0xffffu;
+            val[3] = v.y >> 16;
+        } else {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const unsigned int*>(a.values) + p));
+            val[0] = v.x;
+            val[1] = v.y;
+            val[2] = v.z;
+            val[3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            int c;
+            uint32_t v;
+            load_window<BF, SMX>(a, p + u - lane, end, lane, c, v);  // nonzero p + u
+            col[u] = c;
+            val[u] = v;
+        }
+    }
+}
+
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK = false, bool TM = false,
+          bool SMX = false, bool VL = false>
 __global__ void __launch_bounds__(W * 32, MB)
     spmm_kernel(const __grid_constant__ CUtensorMap tmB, const SpmmArgs a) {
-    using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS>;
+    using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS, TM, VL>;
     constexpr int NCH = C_::NCH, NW = C_::NW;
     constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, ENTRY = C_::ENTRY;
     constexpr bool ADDR = C_::ADDR;
+    // TM: the last TR rows of every chunk are also copied into tensor memory
+    // (replicated in the four subpartitions: lane t of every subpartition
+    // holds the lane's 8 fp32 of each row, columns 8·row .. 8·row+7), and
+    // nonzeros in those rows read B from there instead of shared memory.
+    constexpr int TR = TM ? 64 : 0;
+    constexpr int KL = KC - TR;  // chunk rows read from shared memory
+    static_assert(!TM || (!BF && L == 32 && VEC == 8 && NS == 1 && MB == 1 && KC > TR && TR % W == 0),
+                  "tensor-memory rows: fp32, 32 lanes x 8 columns, one stage, one CTA per SM");
+    static_assert(!VL || (G == 1 && !TM), "vector windows: one lane group, no tensor-memory rows");
 
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
-    int* kr = reinterpret_cast<int*>(smem + NS * STAGE + 16);  // [0]=min col, [1]=max col, [2]=abort
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE);  // [0..1] TMA, [4] TMEM copies
+    int* kr = reinterpret_cast<int*>(smem + NS * STAGE + 16);  // [0]=min col, [1]=max col, [2]=abort, [3]=TMEM base
     unsigned char* lists = smem + NS * STAGE + 64;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,12 +241,16 @@ __global__ void __launch_bounds__(W * 32, MB)
                             (c_lo + j) * KC + b * C_::BOX_ROWS, bar);
     };
 
+    if constexpr (TM) {
+        if (warp == 0) tmem_alloc(smem_addr(&kr[3]), 512);
+    }
     if (threadIdx.x == 0) {
         kr[0] = INT_MAX;
         kr[1] = -1;
         kr[2] = 0;
         mbar_init(smem_addr(&bars[0]), 1);
         mbar_init(smem_addr(&bars[1]), 1);
+        if (TM) mbar_init(smem_addr(&bars[4]), W);  // one commit per warp and chunk
         fence_barrier_init();
         prefetch_tensor_map(&tmB);
         if (whole) {
@@ -191,6 +275,7 @@ __global__ void __launch_bounds__(W * 32, MB)
             }
         }
     }
+    if (TM) tmem_fence_before_sync();
     if (whole) {
         __syncthreads();  // barrier and flag initialisation visible to every thread
     } else {
@@ -221,6 +306,24 @@ __global__ void __launch_bounds__(W * 32, MB)
         }
     }
 
+    // SMX: each row's softmax statistics (warp-cooperative, while the first
+    // chunk's copy is in flight); lane i keeps row slot i's.
+    float my_m = 0.f, my_rz = 0.f;
+    if constexpr (SMX) {
+#pragma unroll 1
+        for (int i = 0; i < R; ++i) {
+            float m, rz;
+            row_softmax_stats(reinterpret_cast<const float*>(a.values), __shfl_sync(kFullMask, my_start, i),
+                              __shfl_sync(kFullMask, my_end, i), lane, m, rz);
+            if (lane == i) {
+                my_m = m;
+                my_rz = rz;
+            }
+        }
+    }
+    // The window of row slot `slot` from position pos (warp-wide call).
+    auto window = [&](int, int pos, int end, int& col, uint32_t& val) { load_window<BF, SMX>(a, pos, end, lane, col, val); };
+
     float acc[R][VEC];
     float acc_hi[LONGK ? R : 1][LONGK ? VEC : 1];  // LONGK: totals of whole 64-chunk runs
 #pragma unroll
@@ -245,26 +348,245 @@ __global__ void __launch_bounds__(W * 32, MB)
     int wcol[RW];
     uint32_t wval[RW];
     int wb[RW];
+    // VL: 128-entry windows (4 entries a lane), from the 16-byte-aligned floor
+    // of the cursor.  (Each form's arrays are dead in the other and compiled away.)
+    int wcv[RW][4];
+    uint32_t wvv[RW][4];
+    int wbv[RW];
+    auto window_v = [&](int, int pos, int end, int (&col)[4], uint32_t (&val)[4]) {
+        load_window_v<BF, SMX>(a, pos, end, lane, col, val);
+    };
+    if constexpr (VL) {
 #pragma unroll
-    for (int i = 0; i < RW; ++i) {
-        wb[i] = __shfl_sync(kFullMask, cur, i);
-        load_window<BF>(a, wb[i], __shfl_sync(kFullMask, my_end, i), lane, wcol[i], wval[i]);
+        for (int i = 0; i < RW; ++i) {
+            wbv[i] = __shfl_sync(kFullMask, cur, i) & ~3;
+            window_v(i, wbv[i], __shfl_sync(kFullMask, my_end, i), wcv[i], wvv[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+            wb[i] = __shfl_sync(kFullMask, cur, i);
+            window(i, wb[i], __shfl_sync(kFullMask, my_end, i), wcol[i], wval[i]);
+        }
     }
 
-    unsigned char* wl = lists + warp * 32 * ENTRY;
+    unsigned char* wl = lists + warp * C_::LIST_SLOTS * ENTRY;
     const uint32_t wl_addr = smem_addr(wl);
+    uint32_t tlane = 0;  // TM: this warp's TMEM lanes, column 0
+    if constexpr (TM) {
+        tmem_fence_after_sync();
+        tlane = (uint32_t)kr[3] + ((uint32_t)(32 * (warp & 3)) << 16);
+    }
 
     for (int j = 0; j < nchunks; ++j) {
         const int s = j % NS;
         const int k0 = (c_lo + j) * KC;
-        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs);
+        // Warp-uniform: the row loop below is full of warp-wide operations.
+        bool ok = __all_sync(kFullMask, mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs));
         if (!ok) kr[2] = 1;
         const uint32_t stage0 = smem_addr(stages + s * STAGE);
         const uint32_t lane_off = l * (NCH ? 16 : 8);
         const uint32_t stage = stage0 + lane_off;
+        bool tm_ready = false, tm_failed = false;  // TM: this chunk's tensor-memory rows have landed
+        if constexpr (TM) {
+            // The chunk is in shared memory: each warp copies its TR/W rows of
+            // the tensor-memory part (two 512-byte halves a row) and commits.
+            if (ok && lane == 0) {
+#pragma unroll
+                for (int q = 0; q < TR / W; ++q) {
+                    const int rr = warp * (TR / W) + q;
+                    tmem_cp_512b_x4((uint32_t)kr[3] + 8 * rr, stage0 + (KL + rr) * PITCH);
+                    tmem_cp_512b_x4((uint32_t)kr[3] + 8 * rr + 4, stage0 + (KL + rr) * PITCH + 512);
+                }
+                tmem_commit(smem_addr(&bars[4]));
+            }
+        }
         if (ok) {
 #pragma unroll
             for (int i = 0; i < R; ++i) {
+                // SMX: this row's softmax statistics, for the list entries.
+                const float row_m = SMX ? __shfl_sync(kFullMask, my_m, i) : 0.f;
+                const float row_rz = SMX ? __shfl_sync(kFullMask, my_rz, i) : 0.f;
+                if constexpr (VL) {
+                    // The row's entries in this chunk, 128-entry windows at a time.
+                    int rc = __shfl_sync(kFullMask, cur, i);
+                    const int re = __shfl_sync(kFullMask, my_end, i);
+                    int vc[4];
+                    uint32_t vv[4];
+                    int base = wbv[PERSIST ? i : 0];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        vc[u] = wcv[PERSIST ? i : 0][u];
+                        vv[u] = wvv[PERSIST ? i : 0][u];
+                    }
+                    if constexpr (!PERSIST) {
+                        if (i + 1 < R) {  // the next row slot's window, fetched while this one computes
+                            wbv[0] = __shfl_sync(kFullMask, cur, i + 1) & ~3;
+                            window_v(i + 1, wbv[0], __shfl_sync(kFullMask, my_end, i + 1), wcv[0], wvv[0]);
+                        }
+                    }
+                    float c4[BF ? 1 : VEC], cc[BF ? 1 : VEC];
+#pragma unroll
+                    for (int v = 0; v < (BF ? 1 : VEC); ++v) c4[v] = cc[v] = 0.f;
+                    while (true) {
+                        // Entry e = 4·lane + u of the window is valid from the
+                        // cursor (e >= wo: the aligned floor's residue is masked)
+                        // to the row end, inside the chunk: a contiguous run.
+                        const int wo = rc - base;  // 0 <= wo < 128
+                        unsigned bal[4];
+                        int n = 0;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int e = 4 * lane + u;
+                            bal[u] = __ballot_sync(kFullMask, e >= wo && base + e < re &&
+                                                                  (unsigned)(vc[u] - k0) < (unsigned)KC);
+                            n += __popc(bal[u]);
+                        }
+                        if (n == 0) break;
+                        const bool more = wo + n == 128;  // the run reaches the window's end
+                        int nc[4];
+                        uint32_t nv[4];
+                        if (more) window_v(i, base + 128, re, nc, nv);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            if ((bal[u] >> lane) & 1u) {
+                                const int slot = 4 * lane + u - wo;
+                                const uint32_t off = (uint32_t)(vc[u] - k0) * PITCH;
+                                const uint32_t vb = value_bits<BF, SMX>(vv[u], row_m, row_rz);
+                                if constexpr (ADDR) {
+                                    reinterpret_cast<uint32_t*>(wl)[slot] = stage0 + off;
+                                    reinterpret_cast<uint16_t*>(wl + 4 * C_::LIST_SLOTS)[slot] = (uint16_t)vb;
+                                } else if constexpr (BF) {
+                                    reinterpret_cast<uint32_t*>(wl)[slot] = (off >> 3) | (vb << 16);
+                                } else {
+                                    reinterpret_cast<uint2*>(wl)[slot] = make_uint2(off, vb);
+                                }
+                            }
+                        }
+                        __syncwarp();
+                        auto load_b = [&](uint32_t p, uint32_t (&w)[NW]) {
+                            if constexpr (NCH == 0) {
+                                const uint2 b = lds64(p);
+                                w[0] = b.x;
+                                w[1] = b.y;
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < NCH; ++c) {
+                                    const uint4 b = lds128(p + C_::piece_off(c));
+                                    w[4 * c] = b.x;
+                                    w[4 * c + 1] = b.y;
+                                    w[4 * c + 2] = b.z;
+                                    w[4 * c + 3] = b.w;
+                                }
+                            }
+                        };
+                        auto step_bf16 = [&](uint32_t ad, uint16_t av) {
+                            uint32_t w[NW];
+                            load_b(ad + lane_off, w);
+#pragma unroll
+                            for (int q = 0; q < NW; ++q) {
+                                acc[i][2 * q] = fma_bf16(av, lo16(w[q]), acc[i][2 * q]);
+                                acc[i][2 * q + 1] = fma_bf16(av, hi16(w[q]), acc[i][2 * q + 1]);
+                            }
+                        };
+                        auto step_f32 = [&](uint32_t off, uint32_t av) {
+                            uint32_t w[NW];
+                            load_b(stage + off, w);
+                            const float x = __uint_as_float(av);
+                            const float2 a2 = make_float2(x, x);
+#pragma unroll
+                            for (int q = 0; q < NW; q += 2) {
+                                float2 c2 = make_float2(c4[q], c4[q + 1]);
+                                c2 = __ffma2_rn(a2, make_float2(__uint_as_float(w[q]), __uint_as_float(w[q + 1])), c2);
+                                c4[q] = c2.x;
+                                c4[q + 1] = c2.y;
+                            }
+                        };
+                        // Runs of at most 32 entries, each into a fresh fp32
+                        // window partial (the same rounding path as 32-entry windows).
+#pragma unroll 1
+                        for (int s0 = 0; s0 < n; s0 += 32) {
+                            const int s1 = min(n, s0 + 32), s4 = s0 + ((s1 - s0) & ~3);
+#pragma unroll 1
+                            for (int t = s0; t < s4; t += 4) {
+                                if constexpr (ADDR) {
+                                    const uint4 ad = lds128(wl_addr + t * 4);
+                                    const uint2 av = lds64(wl_addr + 4 * C_::LIST_SLOTS + t * 2);
+                                    step_bf16(ad.x, lo16(av.x));
+                                    step_bf16(ad.y, hi16(av.x));
+                                    step_bf16(ad.z, lo16(av.y));
+                                    step_bf16(ad.w, hi16(av.y));
+                                } else if constexpr (BF) {
+                                    const uint4 e = lds128(wl_addr + t * 4);
+                                    step_bf16(stage0 + ((e.x & 0xffffu) << 3), hi16(e.x));
+                                    step_bf16(stage0 + ((e.y & 0xffffu) << 3), hi16(e.y));
+                                    step_bf16(stage0 + ((e.z & 0xffffu) << 3), hi16(e.z));
+                                    step_bf16(stage0 + ((e.w & 0xffffu) << 3), hi16(e.w));
+                                } else {
+                                    const uint4 e01 = lds128(wl_addr + t * 8);
+                                    const uint4 e23 = lds128(wl_addr + t * 8 + 16);
+                                    step_f32(e01.x, e01.y);
+                                    step_f32(e01.z, e01.w);
+                                    step_f32(e23.x, e23.y);
+                                    step_f32(e23.z, e23.w);
+                                }
+                            }
+#pragma unroll 1
+                            for (int t = s4; t < s1; ++t) {
+                                if constexpr (ADDR) {
+                                    step_bf16(lds32(wl_addr + t * 4), lds16(wl_addr + 4 * C_::LIST_SLOTS + t * 2));
+                                } else if constexpr (BF) {
+                                    const uint32_t e = lds32(wl_addr + t * 4);
+                                    step_bf16(stage0 + ((e & 0xffffu) << 3), hi16(e));
+                                } else {
+                                    const uint2 e = lds64(wl_addr + t * 8);
+                                    step_f32(e.x, e.y);
+                                }
+                            }
+                            if constexpr (!BF) {
+#pragma unroll
+                                for (int v = 0; v < VEC; ++v) {
+                                    cc[v] += c4[v];
+                                    c4[v] = 0.f;
+                                }
+                            }
+                        }
+                        __syncwarp();
+                        rc += n;
+                        if (!more) break;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            vc[u] = nc[u];
+                            vv[u] = nv[u];
+                        }
+                        base += 128;
+                    }
+                    if constexpr (!BF) {
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) acc[i][v] += cc[v];
+                    }
+                    if constexpr (PERSIST) {
+                        // Half the window used: refill it from the cursor's aligned floor.
+                        if (rc - base >= 64 && rc < re) {
+                            base = rc & ~3;
+                            window_v(i, base, re, vc, vv);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            wcv[i][u] = vc[u];
+                            wvv[i][u] = vv[u];
+                        }
+                        wbv[i] = base;
+                    }
+                    if (lane == i) cur = rc;
+                    if constexpr (!PERSIST) {
+                        if (i + 1 == R) {
+                            wbv[0] = __shfl_sync(kFullMask, cur, 0) & ~3;
+                            window_v(0, wbv[0], __shfl_sync(kFullMask, my_end, 0), wcv[0], wvv[0]);
+                        }
+                    }
+                    continue;
+                }
                 int rc = __shfl_sync(kFullMask, cur, i);
                 const int re = __shfl_sync(kFullMask, my_end, i);
                 int col = wcol[PERSIST ? i : 0];
@@ -273,7 +595,7 @@ __global__ void __launch_bounds__(W * 32, MB)
                 if constexpr (!PERSIST) {
                     if (i + 1 < R) {
                         wb[0] = __shfl_sync(kFullMask, cur, i + 1);
-                        load_window<BF>(a, wb[0], __shfl_sync(kFullMask, my_end, i + 1), lane, wcol[0], wval[0]);
+                        window(i + 1, wb[0], __shfl_sync(kFullMask, my_end, i + 1), wcol[0], wval[0]);
                     }
                 }
                 float c4[BF ? 1 : VEC];  // fp32: this window's partial sums (≤ 32 terms)
@@ -288,32 +610,46 @@ __global__ void __launch_bounds__(W * 32, MB)
                     const unsigned run = __ballot_sync(kFullMask, valid) >> wo;
                     const int n = (run == kFullMask) ? 32 : (__ffs(~run) - 1);
                     if (n == 0) break;
+                    // TM: the run's first n_sm entries lie in the shared-memory
+                    // rows of the chunk, the rest in its tensor-memory rows.
+                    int n_sm = n;
+                    if constexpr (TM) {
+                        const unsigned sm_run =
+                            __ballot_sync(kFullMask, valid && (unsigned)(col - k0) < (unsigned)KL) >> wo;
+                        n_sm = (sm_run == kFullMask) ? 32 : (__ffs(~sm_run) - 1);
+                    }
                     // The window runs out inside this chunk: fetch the next one
                     // now so its latency overlaps this window's work.
                     const bool more = wo + n == 32;
                     int ncol = INT_MAX;
                     uint32_t nval = 0;
-                    if (more) load_window<BF>(a, base + 32, re, lane, ncol, nval);
+                    if (more) window(i, base + 32, re, ncol, nval);
                     // G == 1: exact count (0-3 single steps at the end).  G > 1: each
                     // group's block must start 16-byte aligned for the 128-bit
                     // entry loads, so pad to a multiple of 4·G.  Lane e writes
                     // list slot (e - wo) mod 32: every slot below npad is written.
                     const int npad = (G == 1) ? n : (n + 4 * G - 1) / (4 * G) * (4 * G);
                     const int slot = (lane - wo) & 31;
-                    if (slot < npad) {
+                    const uint32_t vb = value_bits<BF, SMX>(val, row_m, row_rz);
+                    if (TM && slot >= n_sm && slot < n) {
+                        // Tensor-memory rows: (TMEM address, value) in the second
+                        // region, from its first slot, so it reads 16 bytes at a time.
+                        reinterpret_cast<uint2*>(wl)[32 + slot - n_sm] =
+                            make_uint2(tlane + (uint32_t)(col - k0 - KL) * 8u, vb);
+                    } else if (slot < npad) {
                         const bool live = slot < n;
                         const uint32_t off = live ? (uint32_t)(col - k0) * PITCH : 0u;
                         if constexpr (ADDR) {
                             reinterpret_cast<uint32_t*>(wl)[slot] = stage0 + off;
-                            reinterpret_cast<uint16_t*>(wl + 128)[slot] = live ? (uint16_t)val : (uint16_t)0;
+                            reinterpret_cast<uint16_t*>(wl + 128)[slot] = live ? (uint16_t)vb : (uint16_t)0;
                         } else if constexpr (BF) {
-                            reinterpret_cast<uint32_t*>(wl)[slot] = live ? ((off >> 3) | (val << 16)) : 0u;
+                            reinterpret_cast<uint32_t*>(wl)[slot] = live ? ((off >> 3) | (vb << 16)) : 0u;
                         } else {
-                            reinterpret_cast<uint2*>(wl)[slot] = live ? make_uint2(off, val) : make_uint2(0u, 0u);
+                            reinterpret_cast<uint2*>(wl)[slot] = live ? make_uint2(off, vb) : make_uint2(0u, 0u);
                         }
                     }
                     __syncwarp();
-                    const int q = npad / G;  // steps of each group
+                    const int q = (TM ? n_sm : npad) / G;  // steps of each group (TM: shared-memory part)
                     const int q4 = q & ~3;
                     const uint32_t gl = wl_addr + g * q * (ADDR ? 4 : ENTRY);  // ADDR: addresses
                     const uint32_t gv = wl_addr + 128 + g * q * 2;             // ADDR: values
@@ -344,10 +680,8 @@ __global__ void __launch_bounds__(W * 32, MB)
                             acc[i][2 * q + 1] = fma_bf16(av, hi16(w[q]), acc[i][2 * q + 1]);
                         }
                     };
-                    // One fp32 step: staged row at byte offset off, value bits av.
-                    auto step_f32 = [&](uint32_t off, uint32_t av) {
-                        uint32_t w[NW];
-                        load_b(stage + off, w);
+                    // fp32 FMAs of one step: the lane's words w of the B row, value bits av.
+                    auto fma_f32 = [&](const uint32_t (&w)[NW], uint32_t av) {
                         const float x = __uint_as_float(av);
                         const float2 a2 = make_float2(x, x);
 #pragma unroll
@@ -357,6 +691,12 @@ __global__ void __launch_bounds__(W * 32, MB)
                             c4[q] = c2.x;
                             c4[q + 1] = c2.y;
                         }
+                    };
+                    // One fp32 step: staged row at byte offset off, value bits av.
+                    auto step_f32 = [&](uint32_t off, uint32_t av) {
+                        uint32_t w[NW];
+                        load_b(stage + off, w);
+                        fma_f32(w, av);
                     };
 #pragma unroll 1
 #pragma unroll 1
@@ -395,6 +735,88 @@ __global__ void __launch_bounds__(W * 32, MB)
                             step_f32(e.x, e.y);
                         }
                     }
+                    if constexpr (TM) {
+                        // Entries n_sm..n-1: B rows from tensor memory, once this
+                        // chunk's copies have landed (checked once per chunk).
+                        if (n_sm < n && !tm_ready && !tm_failed) {
+                            tm_ready = __all_sync(kFullMask, mbar_wait_bounded(smem_addr(&bars[4]), j & 1, kWaitLimitNs));
+                            tm_failed = !tm_ready;
+                            if (tm_failed) kr[2] = 1;
+                            tmem_fence_after_sync();
+                        }
+                        if (tm_ready && USM_TM_PIPE) {
+                            // Pairs of entries, software-pipelined: the next pair's
+                            // loads are in flight while the current pair's FMAs run
+                            // (the wait covers every outstanding load, so the loads
+                            // of one pair and the FMAs of the previous alternate).
+                            int t = 0, cnt = n - n_sm;
+                            auto ent = [&](int k) { return lds64(wl_addr + (32 + k) * 8); };
+                            if (cnt >= 2) {
+                                uint32_t wa0[NW], wa1[NW], wb0[NW], wb1[NW];
+                                uint2 ea0 = ent(t), ea1 = ent(t + 1);
+                                tmem_ld8x2_nowait(ea0.x, ea1.x, wa0, wa1, c4);
+                                tmem_wait_tied(wa0, wa1, c4);
+                                t += 2;
+                                cnt -= 2;
+#pragma unroll 1
+                                for (; cnt >= 4; cnt -= 4, t += 4) {
+                                    const uint2 eb0 = ent(t), eb1 = ent(t + 1);
+                                    tmem_ld8x2_nowait(eb0.x, eb1.x, wb0, wb1, c4);
+                                    fma_f32(wa0, ea0.y);
+                                    fma_f32(wa1, ea1.y);
+                                    tmem_wait_tied(wb0, wb1, c4);
+                                    ea0 = ent(t + 2);
+                                    ea1 = ent(t + 3);
+                                    tmem_ld8x2_nowait(ea0.x, ea1.x, wa0, wa1, c4);
+                                    fma_f32(wb0, eb0.y);
+                                    fma_f32(wb1, eb1.y);
+                                    tmem_wait_tied(wa0, wa1, c4);
+                                }
+                                if (cnt >= 2) {
+                                    const uint2 eb0 = ent(t), eb1 = ent(t + 1);
+                                    tmem_ld8x2_nowait(eb0.x, eb1.x, wb0, wb1, c4);
+                                    fma_f32(wa0, ea0.y);
+                                    fma_f32(wa1, ea1.y);
+                                    tmem_wait_tied(wb0, wb1, c4);
+                                    fma_f32(wb0, eb0.y);
+                                    fma_f32(wb1, eb1.y);
+                                    t += 2;
+                                    cnt -= 2;
+                                } else {
+                                    fma_f32(wa0, ea0.y);
+                                    fma_f32(wa1, ea1.y);
+                                }
+                            }
+                            if (cnt == 1) {
+                                const uint2 e = ent(t);
+                                uint32_t w[NW];
+                                tmem_ld8(e.x, w);
+                                fma_f32(w, e.y);
+                            }
+                        }
+                        if (tm_ready && !USM_TM_PIPE) {
+                            const uint32_t tl = wl_addr + 32 * 8;  // tensor-memory entries
+                            const int m = n - n_sm;
+                            int t = 0;
+#pragma unroll 1
+                            for (; t + 4 <= m; t += 4) {
+                                const uint4 e01 = lds128(tl + t * 8), e23 = lds128(tl + t * 8 + 16);
+                                uint32_t w0[NW], w1[NW], w2[NW], w3[NW];
+                                tmem_ld8x4(e01.x, e01.z, e23.x, e23.z, w0, w1, w2, w3);
+                                fma_f32(w0, e01.y);
+                                fma_f32(w1, e01.w);
+                                fma_f32(w2, e23.y);
+                                fma_f32(w3, e23.w);
+                            }
+#pragma unroll 1
+                            for (; t < m; ++t) {
+                                const uint2 e = lds64(tl + t * 8);
+                                uint32_t w[NW];
+                                tmem_ld8(e.x, w);
+                                fma_f32(w, e.y);
+                            }
+                        }
+                    }
                     __syncwarp();
                     if constexpr (!BF) {
 #pragma unroll
@@ -419,7 +841,7 @@ __global__ void __launch_bounds__(W * 32, MB)
                     // go by.
                     if (rc - base >= 16 && rc < re) {
                         base = rc;
-                        load_window<BF>(a, rc, re, lane, col, val);
+                        window(i, rc, re, col, val);
                     }
                     wcol[i] = col;
                     wval[i] = val;
@@ -428,8 +850,8 @@ __global__ void __launch_bounds__(W * 32, MB)
                 if (lane == i) cur = rc;
                 if constexpr (!PERSIST) {
                     if (i + 1 == R)
-                        load_window<BF>(a, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), lane,
-                                        wcol[0], wval[0]);
+                        window(0, __shfl_sync(kFullMask, cur, 0), __shfl_sync(kFullMask, my_end, 0), wcol[0],
+                               wval[0]);
                 }
             }
         }
@@ -444,12 +866,28 @@ __global__ void __launch_bounds__(W * 32, MB)
                     }
             }
         }
+        if constexpr (TM) {
+            // Every copy of this chunk has completed before the stage is refilled
+            // (and the barrier's phase is consumed by every warp).
+            if (ok && !tm_ready && !tm_failed && !mbar_wait_bounded(smem_addr(&bars[4]), j & 1, kWaitLimitNs))
+                kr[2] = 1;
+            tmem_fence_before_sync();
+        }
         __syncthreads();  // every warp is done with stage s
+        if (TM) tmem_fence_after_sync();
         if (kr[2]) break;
         if (threadIdx.x == 0 && j + NS < nchunks) {
             fence_proxy_async_smem();
             issue(j + NS);
         }
+    }
+
+    if constexpr (TM) {
+        // Every warp is past its last tensor-memory read: free the columns.
+        tmem_fence_before_sync();
+        __syncthreads();
+        tmem_fence_after_sync();
+        if (warp == 0) tmem_dealloc((uint32_t)kr[3], 512);
     }
 
     if (kr[2]) {
