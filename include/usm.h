@@ -352,9 +352,9 @@ int usm_selftest_wait_timeout(long long limit_ns, void *stream);
  * calls (including the general and static-scratch forms) in this process.
  * A field of 0 keeps the library's own choice.
  *   rows_per_warp    row slots per warp, one of 1, 2, 4, 8, 16, 32
- *                    (csr_spmm has kernels for 2 and 4 only: a forced value
- *                    it has none for makes the call return
- *                    USM_ERR_UNSUPPORTED);
+ *                    (csr_spmm has kernels for 2 and 4, and for 4 and 8 on
+ *                    fp32 masks under 7% set with N > 64: a forced value it
+ *                    has none for makes the call return USM_ERR_UNSUPPORTED);
  *   tiles_per_block  row tiles per diagonal block of the schedule (raised to
  *                    the fewest that hold a block, if below);
  *   k_splits         csr_sddmm: ranges of K chunks, one CTA each (split

@@ -559,6 +559,29 @@ def test_spmm_schedules_do_not_change_bits(usm, schedule, dtype, N, seg):
     assert_within(outs[0], ref, S, TOL[dtype], "spmm under forced schedules")
 
 
+@pytest.mark.parametrize("N", [100, 300])
+def test_spmm_sparse_mask_schedules_do_not_change_bits(usm, schedule, N):
+    """fp32 masks under 7% set run 128-wide strips with 4 or 8 rows a warp:
+    every forced schedule gives the same bits, and the oracle's result."""
+    M, K = 900, 3000
+    csr = W.random_csr([M, K, N, 146], M, K, 0.03)
+    B = W.dense(np.random.default_rng(147), K, N)
+    rod, cid, vd = csr_dev(csr)
+    Bd = dev(B)
+    perm = usm.row_swizzle(rod, K)
+    outs = []
+    for r, t, s_ in [(0, 0, 0), (4, 0, 0), (8, 0, 0), (8, 20, 0), (4, 9, 0), (0, 30, 0)]:
+        schedule(r, t, s_)
+        outs.append(host(usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm)))
+    for c in outs[1:]:
+        assert np.array_equal(c, outs[0])
+    schedule(2, 0, 0)  # no kernel with 2 rows a warp for these masks
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm)
+    ref, S = oracle_spmm(csr, B, "f32")
+    assert_within(outs[0], ref, S, TOL["f32"], "sparse-mask spmm")
+
+
 def test_spmm_rejects_schedules_it_has_no_kernel_for(usm, schedule):
     csr = W.random_csr(144, 100, 200, 0.1)
     rod, cid, vd = csr_dev(csr)

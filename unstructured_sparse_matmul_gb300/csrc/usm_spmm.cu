@@ -148,8 +148,21 @@ template <bool SMX>
 int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
     if (!bf16) {
+#ifndef USM_SPMM_HS_PCT
+#define USM_SPMM_HS_PCT 7
+#endif
+        const long long kspan = a.seg_rows < a.M ? min(a.K, a.seg_rows) : a.K;  // columns a row block spans
+        // Sparse masks (under USM_SPMM_HS_PCT% set): up to 8 rows a warp on
+        // 128-wide strips: 128-row tiles halve the staged rows a nonzero costs
+        // and 384-row chunks double the nonzeros a (row, chunk) visit covers,
+        // at the same registers.  Measured against 256-wide strips with up to 4
+        // rows a warp: FFN 95% 6-11% faster, 90% -2..+3%, LSTM even.
+        const bool sparse = 100LL * a.nnz < (long long)USM_SPMM_HS_PCT * a.M * kspan;
         if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
-        if (a.N <= 128) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
+        if (a.N <= 128) {
+            if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
+            return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
+        }
 #ifndef USM_SPMM_TMEM
 #define USM_SPMM_TMEM 1
 #endif
@@ -163,14 +176,24 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         // rows of every chunk also go to tensor memory (measured on the FFN
         // launches at 70% sparsity: 5-9% faster; at 80% even; 10-20% slower at
         // 90-95%, where the copies and their waits are not paid back).
-        const long long kspan = a.seg_rows < a.M ? min(a.K, a.seg_rows) : a.K;  // columns a row block spans
+#ifndef USM_TM_KC
+#define USM_TM_KC (96 * F)
+#endif
         if (!SMX && USM_SPMM_TMEM && NS == 1 &&
             100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * a.M * kspan)
-            return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
+            return launch_pick<false, 32, 8, W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
+        if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
         return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
     }
     if (a.N <= 64) return launch_pick<true, 16, 4, W, 384 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
-    if (a.N <= 128) return launch_pick<true, 32, 4, W, 192 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
+#ifndef USM_SPMM_HS_BF_PCT
+#define USM_SPMM_HS_BF_PCT 12
+#endif
+    // bf16 on sparse masks with long rows of B (K > 2048): 128-wide strips
+    // (measured: 1024x4096 at 90% 4% faster, at 95% 12%; 4096x1024 1-8% slower).
+    const long long kspan_b = a.seg_rows < a.M ? min(a.K, a.seg_rows) : a.K;
+    if (a.N <= 128 || (kspan_b > 2048 && 100LL * a.nnz < (long long)USM_SPMM_HS_BF_PCT * a.M * kspan_b))
+        return launch_pick<true, 32, 4, W, 192 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
     // 16 bf16 a lane (512-column strips in two TMA boxes, fewer instructions
     // per FMA) measured no faster at 70% and 6-25% slower at 90-95%.
     return launch_pick<true, 32, 8, W, 96 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
