@@ -51,6 +51,8 @@ int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream
 int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream);
 
 size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16);
+// Elements between two strips of SDDMM partials: nnz rounded up to a multiple of 4.
+long long partial_stride(long long nnz);
 int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* workspace,
                  size_t workspace_bytes, cudaStream_t stream);
 int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream);

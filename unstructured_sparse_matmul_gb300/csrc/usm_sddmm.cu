@@ -13,12 +13,12 @@
 namespace usm {
 namespace {
 
-template <bool BF, int L, int VV, int W, int KC, int MINB, int NS>
+template <bool BF, int L, int VV, int W, int KC, int MINB, int NS, bool TM = false>
 int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, cudaStream_t stream) {
     using C_ = SddmmCfg<BF, L, VV, W, KC, MINB, NS>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, Y, BF, a.K, a.D, ldy, C_::DT, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = sddmm_kernel<BF, L, VV, W, KC, MINB, NS>;
+    auto kern = sddmm_kernel<BF, L, VV, W, KC, MINB, NS, TM>;
     static int configured_mask = 0;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -31,11 +31,14 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     const int nstrips = (a.D + C_::DT - 1) / C_::DT;
     if (nstrips > 65535) return USM_ERR_UNSUPPORTED;
     void* final_out = a.out;
+    // Strips of partials lie partial_stride(nnz) elements apart (a multiple of
+    // 4, so every strip starts 16-byte aligned for the strip sum's loads).
+    const long long stride = partial_stride(a.nnz);
     if (nstrips > 1) {
-        if (ws == nullptr || ws_bytes < (size_t)nstrips * (size_t)a.nnz * sizeof(float))
+        if (ws == nullptr || ws_bytes < (size_t)nstrips * (size_t)stride * sizeof(float))
             return USM_ERR_WORKSPACE;
         a.out = ws;
-        a.out_stride = a.nnz;
+        a.out_stride = stride;
     }
     const int sms = sm_count_current_device();
     const long long slots = (long long)sms * MINB;
@@ -106,17 +109,17 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
     if (nstrips > 1) {
         const size_t ob = a.out_bf16 ? 8 : 16, sb = a.scale_bf16 ? 8 : 16;
-        const bool vec = a.nnz % 4 == 0 && (uintptr_t)ws % 16 == 0 && (uintptr_t)final_out % ob == 0 &&
+        const bool vec = (uintptr_t)ws % 16 == 0 && (uintptr_t)final_out % ob == 0 &&
                          (a.scale == nullptr || (uintptr_t)a.scale % sb == 0);
-        const long long items = vec ? a.nnz / 4 : a.nnz;
+        const long long items = vec ? (a.nnz + 3) / 4 : a.nnz;
         long long blocks = (items + 255) / 256;
         if (blocks > 8 * sms) blocks = 8 * sms;
         if (vec)
-            sddmm_strip_sum4_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float4*>(ws), items,
+            sddmm_strip_sum4_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz, stride,
                                                                      nstrips, final_out, a.out_bf16, a.scale,
                                                                      a.scale_bf16);
         else
-            sddmm_strip_sum_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz,
+            sddmm_strip_sum_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz, stride,
                                                                     nstrips, final_out, a.out_bf16, a.scale,
                                                                     a.scale_bf16);
         if (cudaGetLastError() != cudaSuccess) return USM_ERR_CUDA;
@@ -138,11 +141,13 @@ int strip_width(int M, int K, int D, int nnz, bool bf16) {
 
 }  // namespace
 
+long long partial_stride(long long nnz) { return (nnz + 3) / 4 * 4; }
+
 size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16) {
     if (D <= 0 || nnz <= 0) return 0;
     const int dt = strip_width(M, K, D, nnz, bf16);
     const long long nstrips = (D + dt - 1) / dt;
-    return nstrips > 1 ? (size_t)nstrips * (size_t)nnz * sizeof(float) : 0;
+    return nstrips > 1 ? (size_t)nstrips * (size_t)partial_stride(nnz) * sizeof(float) : 0;
 }
 
 
@@ -177,8 +182,15 @@ int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, si
     // fp32: one CTA per SM, up to 128 registers, one 192 KB stage (KC = 384
     // rows of a 128-wide strip, or 192 of a 256-wide one).
     if (!in_bf16) {
+        // 256-wide strips (masks at least a quarter set); USM_SDDMM_TMEM=1 also
+        // reads the last 64 rows of every chunk from tensor memory.
+// Measured 8-16% slower at 70% sparsity (those nonzeros go one a warp step
+// with 8 products a lane, against 4 a step with 32 on the shared-memory path).
+#ifndef USM_SDDMM_TMEM
+#define USM_SDDMM_TMEM 0
+#endif
         if (strip_width(a.M, a.K, a.D, a.nnz, false) == 256)
-            return launch_cfg<false, 8, 8, W, 96 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
+            return launch_cfg<false, 8, 8, W, 96 * F, 1, NS, USM_SDDMM_TMEM && NS == 1>(a, Y, ldy, ws, ws_bytes, stream);
         return launch_cfg<false, 8, 4, W, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
     }
     if (a.D <= 64) return launch_cfg<true, 8, 1, W, 384 * F, 2, NS>(a, Y, ldy, ws, ws_bytes, stream);

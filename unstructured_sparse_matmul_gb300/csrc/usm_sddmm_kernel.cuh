@@ -29,6 +29,15 @@
 //   rounded to nearest even).  With several, each strip writes fp32 partials
 //   to the caller's workspace and a second kernel adds the strips in order:
 //   no atomics, results are bit-reproducible.
+// * Tensor-memory rows (TM, fp32 256-wide strips).  The last 64 rows of every
+//   chunk are also copied into tensor memory (replicated in the four
+//   subpartitions; lane t holds Y[k, 4t..4t+3] and Y[k, 128+4t..131+4t]).
+//   Lane (g, l) of the 8-lane groups already holds, among its X words, the
+//   X values of those columns for t = 8g + l (its words 4g.. and 4(g+4)..),
+//   so a nonzero whose column lies in those rows is taken by the whole warp
+//   at once: one tcgen05.ld per lane, eight products, an 8-lane
+//   transpose-reduction over eight such nonzeros, then the four groups' sums
+//   added with two shuffles.
 #pragma once
 
 #include <climits>
@@ -141,16 +150,20 @@ __device__ __forceinline__ float lane_dot(const uint32_t (&xw)[VV * 4], uint32_t
     }
 }
 
-template <bool BF, int L, int VV, int W, int KC, int MINB, int NS>
+template <bool BF, int L, int VV, int W, int KC, int MINB, int NS, bool TM = false>
 __global__ void __launch_bounds__(W * 32, MINB)
     sddmm_kernel(const __grid_constant__ CUtensorMap tmY, const SddmmArgs a) {
     using C_ = SddmmCfg<BF, L, VV, W, KC, MINB, NS>;
     constexpr int G = C_::G, PITCH = C_::PITCH, STAGE = C_::STAGE, XW = C_::XW;
+    constexpr int TR = TM ? 64 : 0;  // chunk rows also in tensor memory (the last TR)
+    constexpr int KL = KC - TR;      // chunk rows read from shared memory only
+    static_assert(!TM || (!BF && L == 8 && VV == 8 && NS == 1 && MINB == 1 && KC > TR && TR % W == 0),
+                  "tensor-memory rows: fp32 256-wide strips, one stage, one CTA per SM");
 
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
-    int* kr = reinterpret_cast<int*>(smem + NS * STAGE + 16);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * STAGE);  // [0..1] TMA, [4] TMEM copies
+    int* kr = reinterpret_cast<int*>(smem + NS * STAGE + 16);  // [0..1] column range, [2] abort, [3] TMEM base
     uint32_t* lists = reinterpret_cast<uint32_t*>(smem + NS * STAGE + 64);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -185,12 +198,16 @@ __global__ void __launch_bounds__(W * 32, MINB)
                         bar);
     };
 
+    if constexpr (TM) {
+        if (warp == 0) tmem_alloc(smem_addr(&kr[3]), 512);
+    }
     if (threadIdx.x == 0) {
         kr[0] = INT_MAX;
         kr[1] = -1;
         kr[2] = 0;
         mbar_init(smem_addr(&bars[0]), 1);
         mbar_init(smem_addr(&bars[1]), 1);
+        if (TM) mbar_init(smem_addr(&bars[4]), W);  // one commit per warp and chunk
         fence_barrier_init();
         prefetch_tensor_map(&tmY);
         if (whole) {
@@ -214,6 +231,7 @@ __global__ void __launch_bounds__(W * 32, MINB)
             }
         }
     }
+    if (TM) tmem_fence_before_sync();
     if (whole) {
         __syncthreads();  // barrier and flag initialisation visible to every thread
     } else {
@@ -266,13 +284,46 @@ __global__ void __launch_bounds__(W * 32, MINB)
     const int my_slot = (lane % G) * L + lane / G;
     const uint32_t gl = smem_addr(wl + g * L);
     const bool single_strip = gridDim.y == 1;
+    uint32_t tlane = 0;  // TM: this warp's tensor-memory lanes, column 0
+    if constexpr (TM) {
+        tmem_fence_after_sync();
+        tlane = (uint32_t)kr[3] + ((uint32_t)(32 * (warp & 3)) << 16);
+    }
+    // The output (or partial) of nonzero p.
+    auto emit = [&](long long p, float v) {
+        if (single_strip) {
+            const float w = a.scale ? v * scale_at(a.scale, a.scale_bf16, p) : v;
+            if (a.out_bf16)
+                reinterpret_cast<uint16_t*>(a.out)[p] = f32_to_bf16_rne(w);
+            else
+                reinterpret_cast<float*>(a.out)[p] = w;
+        } else {
+            reinterpret_cast<float*>(a.out)[(long long)strip * a.out_stride + p] = v;
+        }
+    };
 
     for (int j = 0; j < nchunks; ++j) {
         const int s = j % NS;
         const int k0 = (c_lo + j) * KC;
-        const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs);
+        // Warp-uniform: the row loop below is full of warp-wide operations.
+        const bool ok = __all_sync(kFullMask, mbar_wait_bounded(smem_addr(&bars[s]), (j / NS) & 1, kWaitLimitNs));
         if (!ok) kr[2] = 1;
-        const uint32_t stage = smem_addr(stages + s * STAGE) + l * 16;
+        const uint32_t stage0 = smem_addr(stages + s * STAGE);
+        const uint32_t stage = stage0 + l * 16;
+        bool tm_ready = false, tm_failed = false;  // TM: this chunk's tensor-memory rows have landed
+        if constexpr (TM) {
+            // Each warp copies its TR/W rows of the chunk's tensor-memory part
+            // (two 512-byte halves a row) and commits.
+            if (ok && lane == 0) {
+#pragma unroll
+                for (int q = 0; q < TR / W; ++q) {
+                    const int rr = warp * (TR / W) + q;
+                    tmem_cp_512b_x4((uint32_t)kr[3] + 8 * rr, stage0 + (KL + rr) * PITCH);
+                    tmem_cp_512b_x4((uint32_t)kr[3] + 8 * rr + 4, stage0 + (KL + rr) * PITCH + 512);
+                }
+                tmem_commit(smem_addr(&bars[4]));
+            }
+        }
         if (ok) {
 #pragma unroll 1
             for (int i = 0; i < R; ++i) {
@@ -282,6 +333,21 @@ __global__ void __launch_bounds__(W * 32, MINB)
                 uint32_t xw[XW];
 #pragma unroll
                 for (int q = 0; q < XW; ++q) xw[q] = pxw[q];
+                // TM: the X words for tensor-memory lane 8g + l (words 4g.. and 4(g+4)..).
+                float xs[TM ? 8 : 1];
+                if constexpr (TM) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t lo = xw[q], hi = xw[16 + q];
+#pragma unroll
+                        for (int gg = 1; gg < 4; ++gg) {
+                            lo = g == gg ? xw[4 * gg + q] : lo;
+                            hi = g == gg ? xw[4 * (gg + 4) + q] : hi;
+                        }
+                        xs[q] = __uint_as_float(lo);
+                        xs[4 + q] = __uint_as_float(hi);
+                    }
+                }
                 // Prefetch the next row slot (slot 0 for the next chunk: its
                 // cursor is final once slot 0 has been processed, when R > 1;
                 // for R == 1 the reload after the segment covers it).
@@ -298,51 +364,107 @@ __global__ void __launch_bounds__(W * 32, MINB)
                     const unsigned bal = __ballot_sync(kFullMask, valid);
                     const int n = (bal == kFullMask) ? 32 : (__ffs(~bal) - 1);
                     if (n == 0) break;
+                    // TM: the first n_sm entries lie in the chunk's shared-memory
+                    // rows, the rest in its tensor-memory rows.
+                    int n_sm = n;
+                    if constexpr (TM) {
+                        const unsigned smb = __ballot_sync(kFullMask, valid && (unsigned)(col - k0) < (unsigned)KL);
+                        n_sm = (smb == kFullMask) ? 32 : (__ffs(~smb) - 1);
+                    }
                     // A full window may continue: fetch the next one now so its
                     // latency overlaps this window's work.
                     const int ncol = (n == 32) ? window_col(a, rc + 32, re, lane) : INT_MAX;
-                    wl[my_slot] = (lane < n) ? (uint32_t)(col - k0) * PITCH : 0u;
-                    __syncwarp();
-                    float part[L];
+                    if (n_sm > 0) {
+                        wl[my_slot] = (lane < n_sm) ? (uint32_t)(col - k0) * PITCH : 0u;
+                        __syncwarp();
+                        float part[L];
 #pragma unroll
-                    for (int t4 = 0; t4 < L; t4 += 4) {
-                        if (t4 * G < n) {
-                            const uint4 o4 = lds128(gl + t4 * 4);
-                            const uint32_t off[4] = {o4.x, o4.y, o4.z, o4.w};
+                        for (int t4 = 0; t4 < L; t4 += 4) {
+                            if (t4 * G < n_sm) {
+                                const uint4 o4 = lds128(gl + t4 * 4);
+                                const uint32_t off[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                part[t4 + u] = ((t4 + u) * G < n) ? lane_dot<BF, L, VV>(xw, stage + off[u]) : 0.f;
-                        } else {
+                                for (int u = 0; u < 4; ++u)
+                                    part[t4 + u] = ((t4 + u) * G < n_sm) ? lane_dot<BF, L, VV>(xw, stage + off[u]) : 0.f;
+                            } else {
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) part[t4 + u] = 0.f;
+                                for (int u = 0; u < 4; ++u) part[t4 + u] = 0.f;
+                            }
+                        }
+                        // Transpose-reduce across the L lanes of each group: after it,
+                        // lane l holds the group's sum for step l.
+#pragma unroll
+                        for (int off = L / 2; off >= 1; off >>= 1) {
+                            const bool upper = (l & off) != 0;
+#pragma unroll
+                            for (int q = 0; q < off; ++q) {
+                                const float send = upper ? part[q] : part[q + off];
+                                const float keep = upper ? part[q + off] : part[q];
+                                part[q] = keep + __shfl_xor_sync(kFullMask, send, off);
+                            }
+                        }
+                        const int e = l * G + g;  // window entry whose sum this lane holds
+                        if (e < n_sm) emit((long long)rc + e, part[0]);
+                        __syncwarp();
+                    }
+                    if constexpr (TM) {
+                        // Entries n_sm..n-1, Y rows from tensor memory, once this
+                        // chunk's copies have landed (checked once per chunk).
+                        if (n_sm < n && !tm_ready && !tm_failed) {
+                            tm_ready = __all_sync(kFullMask, mbar_wait_bounded(smem_addr(&bars[4]), j & 1, kWaitLimitNs));
+                            tm_failed = !tm_ready;
+                            if (tm_failed) kr[2] = 1;
+                            tmem_fence_after_sync();
+                        }
+                        if (tm_ready) {
+#pragma unroll 1
+                            for (int t0 = n_sm; t0 < n; t0 += 8) {
+                                // Eight nonzeros, each taken by the whole warp: lane
+                                // 8g + l multiplies its eight Y values by xs.
+                                float tp[8];
+#pragma unroll
+                                for (int hb = 0; hb < 8; hb += 4) {
+                                    uint32_t ad[4];
+#pragma unroll
+                                    for (int b = 0; b < 4; ++b) {
+                                        const int c = __shfl_sync(kFullMask, col, min(t0 + hb + b, n - 1));
+                                        ad[b] = tlane + (uint32_t)(c - k0 - KL) * 8u;
+                                    }
+                                    uint32_t w0[8], w1[8], w2[8], w3[8];
+                                    tmem_ld8x4(ad[0], ad[1], ad[2], ad[3], w0, w1, w2, w3);
+                                    auto dot8 = [&](const uint32_t (&w)[8]) {
+                                        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                                        for (int q = 0; q < 8; q += 2)
+                                            s2 = __ffma2_rn(make_float2(xs[q], xs[q + 1]),
+                                                            make_float2(__uint_as_float(w[q]), __uint_as_float(w[q + 1])), s2);
+                                        return s2.x + s2.y;
+                                    };
+                                    tp[hb] = dot8(w0);
+                                    tp[hb + 1] = dot8(w1);
+                                    tp[hb + 2] = dot8(w2);
+                                    tp[hb + 3] = dot8(w3);
+                                }
+                                // Transpose-reduce over the 8 lanes of each group (lane l
+                                // then holds its group's sum for nonzero t0 + l), then add
+                                // the four groups' sums.
+#pragma unroll
+                                for (int off = 4; off >= 1; off >>= 1) {
+                                    const bool upper = (l & off) != 0;
+#pragma unroll
+                                    for (int q = 0; q < off; ++q) {
+                                        const float send = upper ? tp[q] : tp[q + off];
+                                        const float keep = upper ? tp[q + off] : tp[q];
+                                        tp[q] = keep + __shfl_xor_sync(kFullMask, send, off);
+                                    }
+                                }
+                                float v = tp[0];
+                                v += __shfl_xor_sync(kFullMask, v, 8);
+                                v += __shfl_xor_sync(kFullMask, v, 16);
+                                if (g == 0 && t0 + l < n) emit((long long)rc + t0 + l, v);
+                            }
                         }
                     }
-                    // Transpose-reduce across the L lanes of each group: after it,
-                    // lane l holds the group's sum for step l.
-#pragma unroll
-                    for (int off = L / 2; off >= 1; off >>= 1) {
-                        const bool upper = (l & off) != 0;
-#pragma unroll
-                        for (int q = 0; q < off; ++q) {
-                            const float send = upper ? part[q] : part[q + off];
-                            const float keep = upper ? part[q + off] : part[q];
-                            part[q] = keep + __shfl_xor_sync(kFullMask, send, off);
-                        }
-                    }
-                    const int e = l * G + g;  // window entry whose sum this lane holds
-                    if (e < n) {
-                        const long long p = (long long)rc + e;
-                        if (single_strip) {
-                            const float v = a.scale ? part[0] * scale_at(a.scale, a.scale_bf16, p) : part[0];
-                            if (a.out_bf16)
-                                reinterpret_cast<uint16_t*>(a.out)[p] = f32_to_bf16_rne(v);
-                            else
-                                reinterpret_cast<float*>(a.out)[p] = v;
-                        } else {
-                            reinterpret_cast<float*>(a.out)[(long long)strip * a.out_stride + p] = part[0];
-                        }
-                    }
-                    __syncwarp();
                     rc += n;
                     if (n < 32) break;
                     col = ncol;
@@ -354,12 +476,28 @@ __global__ void __launch_bounds__(W * 32, MINB)
                 }
             }
         }
+        if constexpr (TM) {
+            // Every copy of this chunk has completed before the stage is refilled
+            // (and the barrier's phase is consumed by every warp).
+            if (ok && !tm_ready && !tm_failed && !mbar_wait_bounded(smem_addr(&bars[4]), j & 1, kWaitLimitNs))
+                kr[2] = 1;
+            tmem_fence_before_sync();
+        }
         __syncthreads();
+        if (TM) tmem_fence_after_sync();
         if (kr[2]) break;
         if (threadIdx.x == 0 && j + NS < nchunks) {
             fence_proxy_async_smem();
             issue(j + NS);
         }
+    }
+
+    if constexpr (TM) {
+        // Every warp is past its last tensor-memory read: free the columns.
+        tmem_fence_before_sync();
+        __syncthreads();
+        tmem_fence_after_sync();
+        if (warp == 0) tmem_dealloc((uint32_t)kr[3], 512);
     }
 
     if (kr[2] && threadIdx.x == 0) {
@@ -378,16 +516,17 @@ __global__ void __launch_bounds__(W * 32, MINB)
 // fp32 worst-case rounding bound holds for D up to about 680k columns.
 constexpr int kStripRun = 64;
 
-// out[p] = Σ_s partial[s][p], times the mask's value when scaling.
-__global__ void sddmm_strip_sum_kernel(const float* __restrict__ part, long long nnz, int nstrips,
-                                       void* out, int out_bf16, const void* scale, int scale_bf16) {
+// out[p] = Σ_s partial[s][p] (strip s at part + s·stride), times the mask's
+// value when scaling.
+__global__ void sddmm_strip_sum_kernel(const float* __restrict__ part, long long nnz, long long stride,
+                                       int nstrips, void* out, int out_bf16, const void* scale, int scale_bf16) {
     for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < nnz;
          p += (long long)gridDim.x * blockDim.x) {
         float s = 0.f;
         for (int k0 = 0; k0 < nstrips; k0 += kStripRun) {
-            float t = part[(long long)k0 * nnz + p];
+            float t = part[(long long)k0 * stride + p];
             const int k1 = min(nstrips, k0 + kStripRun);
-            for (int k = k0 + 1; k < k1; ++k) t += part[(long long)k * nnz + p];
+            for (int k = k0 + 1; k < k1; ++k) t += part[(long long)k * stride + p];
             s = k0 == 0 ? t : s + t;
         }
         if (scale) s *= scale_at(scale, scale_bf16, p);
@@ -399,19 +538,23 @@ __global__ void sddmm_strip_sum_kernel(const float* __restrict__ part, long long
 }
 
 // The same sum four nonzeros at a time with 16-byte loads of every strip's
-// partials (nnz a multiple of 4, partials, out and scale aligned to the
-// vector): several loads in flight per thread instead of one.
-__global__ void sddmm_strip_sum4_kernel(const float4* __restrict__ part, long long n4, int nstrips, void* out,
-                                        int out_bf16, const void* scale, int scale_bf16) {
+// partials (stride a multiple of 4; partials, out and scale aligned to the
+// vector): several loads in flight per thread instead of one.  The last
+// group of four may run past nnz: its partials are in the strip's padding
+// and its stores stop at nnz.
+__global__ void sddmm_strip_sum4_kernel(const float* __restrict__ part, long long nnz, long long stride, int nstrips,
+                                        void* out, int out_bf16, const void* scale, int scale_bf16) {
+    const long long n4 = (nnz + 3) / 4, s4 = stride / 4;
+    const float4* __restrict__ part4 = reinterpret_cast<const float4*>(part);
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
          i += (long long)gridDim.x * blockDim.x) {
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int k0 = 0; k0 < nstrips; k0 += kStripRun) {
-            float4 t = __ldcs(part + (long long)k0 * n4 + i);
+            float4 t = __ldcs(part4 + (long long)k0 * s4 + i);
             const int k1 = min(nstrips, k0 + kStripRun);
 #pragma unroll 4
             for (int k = k0 + 1; k < k1; ++k) {
-                const float4 v = __ldcs(part + (long long)k * n4 + i);
+                const float4 v = __ldcs(part4 + (long long)k * s4 + i);
                 t.x += v.x;
                 t.y += v.y;
                 t.z += v.z;
@@ -426,27 +569,39 @@ __global__ void sddmm_strip_sum4_kernel(const float4* __restrict__ part, long lo
                 s.w += t.w;
             }
         }
-        if (scale) {
-            if (scale_bf16) {
-                const uint2 b = __ldg(reinterpret_cast<const uint2*>(scale) + i);
-                s.x *= __uint_as_float(b.x << 16);
-                s.y *= __uint_as_float(b.x & 0xffff0000u);
-                s.z *= __uint_as_float(b.y << 16);
-                s.w *= __uint_as_float(b.y & 0xffff0000u);
-            } else {
-                const float4 c = __ldg(reinterpret_cast<const float4*>(scale) + i);
-                s.x *= c.x;
-                s.y *= c.y;
-                s.z *= c.z;
-                s.w *= c.w;
+        const long long p0 = 4 * i;
+        if (p0 + 4 <= nnz) {
+            if (scale) {
+                if (scale_bf16) {
+                    const uint2 b = __ldg(reinterpret_cast<const uint2*>(scale) + i);
+                    s.x *= __uint_as_float(b.x << 16);
+                    s.y *= __uint_as_float(b.x & 0xffff0000u);
+                    s.z *= __uint_as_float(b.y << 16);
+                    s.w *= __uint_as_float(b.y & 0xffff0000u);
+                } else {
+                    const float4 c = __ldg(reinterpret_cast<const float4*>(scale) + i);
+                    s.x *= c.x;
+                    s.y *= c.y;
+                    s.z *= c.z;
+                    s.w *= c.w;
+                }
             }
-        }
-        if (out_bf16) {
-            const uint32_t lo = (uint32_t)f32_to_bf16_rne(s.x) | ((uint32_t)f32_to_bf16_rne(s.y) << 16);
-            const uint32_t hi = (uint32_t)f32_to_bf16_rne(s.z) | ((uint32_t)f32_to_bf16_rne(s.w) << 16);
-            reinterpret_cast<uint2*>(out)[i] = make_uint2(lo, hi);
-        } else {
-            reinterpret_cast<float4*>(out)[i] = s;
+            if (out_bf16) {
+                const uint32_t lo = (uint32_t)f32_to_bf16_rne(s.x) | ((uint32_t)f32_to_bf16_rne(s.y) << 16);
+                const uint32_t hi = (uint32_t)f32_to_bf16_rne(s.z) | ((uint32_t)f32_to_bf16_rne(s.w) << 16);
+                reinterpret_cast<uint2*>(out)[i] = make_uint2(lo, hi);
+            } else {
+                reinterpret_cast<float4*>(out)[i] = s;
+            }
+        } else {  // the ragged last group: element by element up to nnz
+            const float v[4] = {s.x, s.y, s.z, s.w};
+            for (int u = 0; u < 4 && p0 + u < nnz; ++u) {
+                const float w = scale ? v[u] * scale_at(scale, scale_bf16, p0 + u) : v[u];
+                if (out_bf16)
+                    reinterpret_cast<uint16_t*>(out)[p0 + u] = f32_to_bf16_rne(w);
+                else
+                    reinterpret_cast<float*>(out)[p0 + u] = w;
+            }
         }
     }
 }
