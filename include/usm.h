@@ -362,7 +362,11 @@ int usm_selftest_wait_timeout(long long limit_ns, void *stream);
  *                    csr_spmm accepts only 0 or 1.
  * Results do not depend on the schedule: an SDDMM output adds the same
  * terms in the same order under every schedule, and so does an SpMM output
- * under every schedule of one element type and strip width.  The setting is
+ * under every schedule of one element type and strip width.  While an
+ * override is set, csr_spmm always runs its staged kernels: fp32 masks
+ * under 3% set with N <= 128, which it otherwise serves with a kernel that
+ * gathers the rows of B without staging (and sums in another order), then
+ * give results within the same tolerance but not the same bits.  The setting is
  * process-wide and not ordered with calls issued concurrently on other
  * threads.  Returns USM_ERR_INVALID_ARG (setting unchanged) for a value
  * outside these sets.

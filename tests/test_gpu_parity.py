@@ -561,10 +561,11 @@ def test_spmm_schedules_do_not_change_bits(usm, schedule, dtype, N, seg):
 
 @pytest.mark.parametrize("N", [100, 300])
 def test_spmm_sparse_mask_schedules_do_not_change_bits(usm, schedule, N):
-    """fp32 masks under 7% set run 128-wide strips with 4 or 8 rows a warp:
+    """fp32 masks under 7% set (and, for N <= 128, at least 3%: sparser ones
+    take the gather kernel) run 128-wide strips with 4 or 8 rows a warp:
     every forced schedule gives the same bits, and the oracle's result."""
     M, K = 900, 3000
-    csr = W.random_csr([M, K, N, 146], M, K, 0.03)
+    csr = W.random_csr([M, K, N, 146], M, K, 0.05)
     B = W.dense(np.random.default_rng(147), K, N)
     rod, cid, vd = csr_dev(csr)
     Bd = dev(B)
@@ -580,6 +581,33 @@ def test_spmm_sparse_mask_schedules_do_not_change_bits(usm, schedule, N):
         usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm)
     ref, S = oracle_spmm(csr, B, "f32")
     assert_within(outs[0], ref, S, TOL["f32"], "sparse-mask spmm")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [4, 64, 100, 128])
+def test_spmm_gather_path(usm, schedule, dtype, N):
+    """fp32 masks under 3% set with N <= 128 take the kernel that gathers the rows
+    of B without staging: every element against the oracle, every column
+    pass edge (N = 4, 100) included, and against the staged kernels (run by
+    forcing a schedule) within the same tolerance."""
+    M, K = 3000, 4096
+    lengths = np.random.default_rng([N, 148]).binomial(K, 0.02, M)
+    lengths[:7] = 0
+    lengths[7] = 300   # a row longer than a window of 32
+    csr = W.random_csr([M, K, N, 149], M, K, 0.0, dtype=dtype, lengths=lengths)
+    B = W.dense(np.random.default_rng(150), K, N, 1.0, dtype)
+    rod, cid, vd = csr_dev(csr)
+    Bd = dev(B, dtype)
+    perm = usm.row_swizzle(rod, K)
+    C = host(usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm))
+    ref, S = oracle_spmm(csr, B, dtype)
+    assert_within(C, ref, S, TOL[dtype], f"gather spmm {dtype} N={N}")
+    schedule(4, 0, 0)
+    staged = host(usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm))
+    assert_within(staged, ref, S, TOL[dtype], f"staged spmm {dtype} N={N}")
+    schedule(0, 0, 0)
+    again = host(usm.spmm(rod, cid, vd, Bd, K=K))  # no swizzle: same bits (one row a warp)
+    assert np.array_equal(again, C)
 
 
 def test_spmm_rejects_schedules_it_has_no_kernel_for(usm, schedule):

@@ -144,20 +144,52 @@ int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) 
 
 // The six tile shapes by element type and N.  SMX: the values are the rows'
 // softmax probabilities of fp32 scores (csr_spmm_row_softmax).
+// Direct gather (no staging) for very sparse fp32 masks with narrow rows of
+// B: a mask under USM_SPMM_GATHER_PERMILLE per mille set and N <=
+// USM_SPMM_GATHER_N, unless a launch shape is forced (the staged kernels'
+// schedules are what usm_set_schedule_override controls); with or without
+// the fused softmax, so csr_spmm_row_softmax keeps csr_spmm's bits.  Measured on the
+// LSTM sweep (8192x4096, N = 128): 98% sparsity 25% faster than staging all
+// of K per CTA, 95% 14% slower; FFN 95% (N = 2048) 1.6-4.6x slower.
+#ifndef USM_SPMM_GATHER_PERMILLE
+#define USM_SPMM_GATHER_PERMILLE 30
+#endif
+#ifndef USM_SPMM_GATHER_N
+#define USM_SPMM_GATHER_N 128
+#endif
+template <bool SMX>
+int launch_gather(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
+    const long long warps_needed = a.M;
+    long long blocks = (warps_needed + 7) / 8;
+    const long long cap = 8LL * sm_count_current_device();
+    if (blocks > cap) blocks = cap;
+    spmm_gather_kernel<false, SMX><<<(int)blocks, 256, 0, stream>>>(a, B, ldb);
+    return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
+}
+
 template <bool SMX>
 int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
+    // Every kernel choice below depends on the problem (nnz over M·K, N, the
+    // element type), never on the schedule arguments (swizzle, seg_rows), so
+    // those never change the result.
+    const long long cells = (long long)a.M * a.K;
+    {
+        const ScheduleOverride ov = schedule_override();
+        if (!bf16 && ov.rows_per_warp == 0 && ov.tiles_per_block == 0 && ov.k_splits == 0 &&
+            a.N <= USM_SPMM_GATHER_N && 1000LL * a.nnz < (long long)USM_SPMM_GATHER_PERMILLE * cells)
+            return launch_gather<SMX>(a, B, ldb, stream);
+    }
     if (!bf16) {
 #ifndef USM_SPMM_HS_PCT
 #define USM_SPMM_HS_PCT 7
 #endif
-        const long long kspan = a.seg_rows < a.M ? min(a.K, a.seg_rows) : a.K;  // columns a row block spans
         // Sparse masks (under USM_SPMM_HS_PCT% set): up to 8 rows a warp on
         // 128-wide strips: 128-row tiles halve the staged rows a nonzero costs
         // and 384-row chunks double the nonzeros a (row, chunk) visit covers,
         // at the same registers.  Measured against 256-wide strips with up to 4
         // rows a warp: FFN 95% 6-11% faster, 90% -2..+3%, LSTM even.
-        const bool sparse = 100LL * a.nnz < (long long)USM_SPMM_HS_PCT * a.M * kspan;
+        const bool sparse = 100LL * a.nnz < (long long)USM_SPMM_HS_PCT * cells;
         if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
         if (a.N <= 128) {
             if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
@@ -179,8 +211,7 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #ifndef USM_TM_KC
 #define USM_TM_KC (96 * F)
 #endif
-        if (!SMX && USM_SPMM_TMEM && NS == 1 &&
-            100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * a.M * kspan)
+        if (!SMX && USM_SPMM_TMEM && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
             return launch_pick<false, 32, 8, W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
         if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
         return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
@@ -191,8 +222,7 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #endif
     // bf16 on sparse masks with long rows of B (K > 2048): 128-wide strips
     // (measured: 1024x4096 at 90% 4% faster, at 95% 12%; 4096x1024 1-8% slower).
-    const long long kspan_b = a.seg_rows < a.M ? min(a.K, a.seg_rows) : a.K;
-    if (a.N <= 128 || (kspan_b > 2048 && 100LL * a.nnz < (long long)USM_SPMM_HS_BF_PCT * a.M * kspan_b))
+    if (a.N <= 128 || (a.K > 2048 && 100LL * a.nnz < (long long)USM_SPMM_HS_BF_PCT * cells))
         return launch_pick<true, 32, 4, W, 192 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
     // 16 bf16 a lane (512-column strips in two TMA boxes, fewer instructions
     // per FMA) measured no faster at 70% and 6-25% slower at 90-95%.

@@ -936,6 +936,127 @@ __global__ void __launch_bounds__(W * 32, MB)
     }
 }
 
+// Direct-gather SpMM, for masks so sparse that staging every row of B in
+// each CTA costs more than the nonzeros use (LSTM-like shapes at 98%): no
+// shared memory.  SMX: the values are the rows' softmax probabilities of
+// fp32 scores, formed as in the staged kernel.  Each warp takes rows of the swizzled order (grid-stride),
+// and for every nonzero reads the lane's 16 bytes of the B row (4 fp32 or 8
+// bf16 of a 32·VEC-column pass) straight from global memory, eight
+// nonzeros' loads in flight.  fp32 sums: ≤ 32 terms (one window) into a
+// fresh partial, partials into the row total.  Column indices outside
+// [0, K) read row 0 (undefined result, in-bounds access).
+#ifndef USM_GATHER_MINB
+#define USM_GATHER_MINB 4
+#endif
+template <bool BF, bool SMX = false>
+__global__ void __launch_bounds__(256, USM_GATHER_MINB) spmm_gather_kernel(const SpmmArgs a, const void* __restrict__ Bv, long long ldb) {
+    constexpr int VEC = BF ? 8 : 4;
+    constexpr int ES = BF ? 2 : 4;
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    const unsigned char* B = static_cast<const unsigned char*>(Bv);
+    for (long long m = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; m < a.M; m += warps) {
+        const int r = a.perm ? __ldg(a.perm + m) : (int)m;
+        if ((unsigned)r >= (unsigned)a.M) continue;  // warp-uniform
+        int s = __ldg(a.row_offsets + r), e = __ldg(a.row_offsets + r + 1);
+        s = min(max(s, 0), a.nnz);
+        e = min(max(e, s), a.nnz);
+        float row_m = 0.f, row_rz = 0.f;  // SMX: the row's softmax statistics
+        if constexpr (SMX) row_softmax_stats(reinterpret_cast<const float*>(a.values), s, e, lane, row_m, row_rz);
+        for (int n0 = 0; n0 < a.N; n0 += 32 * VEC) {
+            const int c0 = n0 + lane * VEC;          // the lane's first column
+            const bool full = c0 + VEC <= a.N;       // a whole 16-byte piece
+            const bool any = c0 < a.N;
+            float acc[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+            // The lane's 16 bytes of B row k (zeros past N).
+            auto load_b = [&](int k) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                const unsigned char* row = B + ((long long)k * ldb + c0) * ES;
+                if (full) {
+                    w = __ldg(reinterpret_cast<const uint4*>(row));
+                } else if (any) {
+                    uint32_t h[VEC];
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v)
+                        h[v] = c0 + v < a.N ? (BF ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(row) + v)
+                                                  : __ldg(reinterpret_cast<const unsigned int*>(row) + v))
+                                            : 0u;
+                    if constexpr (BF)
+                        w = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+                    else
+                        w = make_uint4(h[0], h[1], h[2], h[3]);
+                }
+                return w;
+            };
+            auto fma_b = [&](float (&c)[VEC], uint32_t av, uint4 w) {
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                if constexpr (BF) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        c[2 * q] = fma_bf16((uint16_t)av, lo16(ww[q]), c[2 * q]);
+                        c[2 * q + 1] = fma_bf16((uint16_t)av, hi16(ww[q]), c[2 * q + 1]);
+                    }
+                } else {
+                    const float x = __uint_as_float(av);
+                    const float2 a2 = make_float2(x, x);
+#pragma unroll
+                    for (int q = 0; q < 4; q += 2) {
+                        float2 c2 = make_float2(c[q], c[q + 1]);
+                        c2 = __ffma2_rn(a2, make_float2(__uint_as_float(ww[q]), __uint_as_float(ww[q + 1])), c2);
+                        c[q] = c2.x;
+                        c[q + 1] = c2.y;
+                    }
+                }
+            };
+            for (int base = s; base < e; base += 32) {
+                int col;
+                uint32_t val;
+                load_window<BF, SMX>(a, base, e, lane, col, val);
+                col = (unsigned)col < (unsigned)a.K ? col : 0;
+                val = value_bits<BF, SMX>(val, row_m, row_rz);
+                const int n = min(32, e - base);
+                float part[VEC];
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) part[v] = BF ? acc[v] : 0.f;  // bf16: one running sum
+                int t = 0;
+#pragma unroll 1
+                for (; t + 8 <= n; t += 8) {
+                    uint4 w[8];
+                    uint32_t av[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        w[u] = load_b(__shfl_sync(kFullMask, col, t + u));
+                        av[u] = __shfl_sync(kFullMask, val, t + u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) fma_b(part, av[u], w[u]);
+                }
+#pragma unroll 1
+                for (; t < n; ++t) {
+                    const uint4 w = load_b(__shfl_sync(kFullMask, col, t));
+                    fma_b(part, __shfl_sync(kFullMask, val, t), w);
+                }
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) acc[v] = BF ? part[v] : acc[v] + part[v];
+            }
+            if (any) {
+                float* crow = a.C + (long long)r * a.ldc + c0;
+                if (full) {
+#pragma unroll
+                    for (int v = 0; v < VEC; v += 4)
+                        *reinterpret_cast<float4*>(crow + v) = make_float4(acc[v], acc[v + 1], acc[v + 2], acc[v + 3]);
+                } else {
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v)
+                        if (c0 + v < a.N) crow[v] = acc[v];
+                }
+            }
+        }
+    }
+}
+
 __global__ void fill_f32_kernel(float* C, int M, int N, long long ldc) {
     const long long total = (long long)M * N;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
