@@ -146,6 +146,39 @@ def test_spmm_leading_dimensions(usm):
     assert np.all(C[:, N:] == 0), "wrote outside the N columns"
 
 
+@pytest.mark.parametrize("M,K,N,density,seg", [(900, 500, 300, 0.4, 0), (700, 2500, 257, 0.3, 0),
+                                                (1000, 1000, 512, 0.6, 500), (300, 4097, 600, 0.3, 0)])
+def test_spmm_tensor_memory_rows(usm, schedule, M, K, N, density, seg):
+    """fp32 masks at least a quarter set with N > 128 read the last 64 rows
+    of every 192-row chunk from tensor memory: ragged last chunks (K not a
+    multiple of 192: some of those rows lie past K), several and ragged
+    strips, block-diagonal schedules and forced schedules, every element
+    against the oracle and forced schedules bit for bit."""
+    if seg:
+        K = M
+        rng = np.random.default_rng([M, 151])
+        lengths = rng.binomial(seg, density, M)
+        base = (np.arange(M) // seg) * seg
+        ro, ci = W.csr_from_lengths(rng, lengths, seg, col_base=base)
+        csr = W.CSR(M, K, ro, ci, W.values_for(rng, int(ro[-1]), 1.0, "f32"), "f32", seg_rows=seg)
+    else:
+        csr = W.random_csr([M, K, N, 152], M, K, density)
+    assert csr.nnz >= 0.25 * M * K
+    B = W.dense(np.random.default_rng([M, K, 153]), K, N)
+    rod, cid, vd = csr_dev(csr)
+    Bd = dev(B)
+    perm = usm.row_swizzle(rod, K, seg)
+    outs = []
+    for r, t, s_ in [(0, 0, 0), (2, 0, 0), (4, 0, 0), (0, 40, 0)]:
+        schedule(r, t, s_)
+        outs.append(host(usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm, seg_rows=seg)))
+    for c in outs[1:]:
+        assert np.array_equal(c, outs[0])
+    ref, S = oracle_spmm(csr, B, "f32")
+    assert_within(outs[0], ref, S, TOL["f32"], f"tensor-memory spmm {M}x{K}x{N}")
+    assert usm.poll_status() == 0
+
+
 def test_spmm_long_k_fp32(usm):
     """fp32 with more than 128 chunks of K (K = 40000: 209 chunks of 192
     rows) takes the kernel with a second-level accumulator; with every

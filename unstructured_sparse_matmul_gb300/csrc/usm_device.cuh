@@ -142,6 +142,30 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&w)[8]) {
         : "r"(taddr)
         : "memory");
 }
+// Four loads of four columns (16 bytes a lane) behind one wait.
+__device__ __forceinline__ void tmem_ld4x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint4& w0, uint4& w1,
+                                           uint4& w2, uint4& w3) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%4,%5,%6,%7}, [%17];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%8,%9,%10,%11}, [%18];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%12,%13,%14,%15}, [%19];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w), "=r"(w1.x), "=r"(w1.y), "=r"(w1.z), "=r"(w1.w),
+          "=r"(w2.x), "=r"(w2.y), "=r"(w2.z), "=r"(w2.w), "=r"(w3.x), "=r"(w3.y), "=r"(w3.z), "=r"(w3.w)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3)
+        : "memory");
+}
+__device__ __forceinline__ uint4 tmem_ld4(uint32_t a) {
+    uint4 w;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+        : "r"(a)
+        : "memory");
+    return w;
+}
 // Two loads of eight columns issued without a wait (results are not ready
 // until tmem_wait_tied).  The accumulators c are tied in so that FMAs on
 // them that come after this call in program order stay after the loads.

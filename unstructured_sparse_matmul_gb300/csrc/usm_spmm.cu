@@ -226,6 +226,18 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         return launch_pick<true, 32, 4, W, 192 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
     // 16 bf16 a lane (512-column strips in two TMA boxes, fewer instructions
     // per FMA) measured no faster at 70% and 6-25% slower at 90-95%.
+// bf16 rows in tensor memory (256 columns for each of the two CTAs an SM
+// holds, one tcgen05.ld.x4 a nonzero): measured 8-17% slower at 70% sparsity
+// and even at 80% (two CTAs of 64 registers do not hide the loads' waits),
+// so off by default.
+#ifndef USM_SPMM_TMEM_BF
+#define USM_SPMM_TMEM_BF 0
+#endif
+#ifndef USM_TM_RB_BF
+#define USM_TM_RB_BF 4
+#endif
+    if (!SMX && USM_SPMM_TMEM_BF && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
+        return launch_pick<true, 32, 8, W, 96 * F, NS, 2, 2, USM_TM_RB_BF, NS == 1>(a, B, ldb, stream);
     return launch_pick<true, 32, 8, W, 96 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
 }
 

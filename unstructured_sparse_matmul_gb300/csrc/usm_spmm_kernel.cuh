@@ -205,10 +205,16 @@ __global__ void __launch_bounds__(W * 32, MB)
     // (replicated in the four subpartitions: lane t of every subpartition
     // holds the lane's 8 fp32 of each row, columns 8·row .. 8·row+7), and
     // nonzeros in those rows read B from there instead of shared memory.
+    // fp32: 8 columns a row (two 512-byte halves), all 512 columns of the SM;
+    // bf16: 4 columns a row (one 512-byte row), 256 columns for each of the
+    // two CTAs an SM holds.
     constexpr int TR = TM ? 64 : 0;
     constexpr int KL = KC - TR;  // chunk rows read from shared memory
-    static_assert(!TM || (!BF && L == 32 && VEC == 8 && NS == 1 && MB == 1 && KC > TR && TR % W == 0),
-                  "tensor-memory rows: fp32, 32 lanes x 8 columns, one stage, one CTA per SM");
+    constexpr int TCPR = BF ? 4 : 8;         // tensor-memory columns a row
+    constexpr uint32_t TCOLS = BF ? 256 : 512;  // columns allocated
+    static_assert(!TM || (L == 32 && VEC == 8 && NS == 1 && MB == (BF ? 2 : 1) && KC > TR && TR % W == 0 &&
+                          TR * TCPR == (int)TCOLS),
+                  "tensor-memory rows: 32 lanes x 16 or 32 bytes, one stage, 1 (fp32) or 2 (bf16) CTAs per SM");
     static_assert(!VL || (G == 1 && !TM), "vector windows: one lane group, no tensor-memory rows");
 
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(W * 32, MB)
     };
 
     if constexpr (TM) {
-        if (warp == 0) tmem_alloc(smem_addr(&kr[3]), 512);
+        if (warp == 0) tmem_alloc(smem_addr(&kr[3]), TCOLS);
     }
     if (threadIdx.x == 0) {
         kr[0] = INT_MAX;
@@ -395,8 +401,8 @@ __global__ void __launch_bounds__(W * 32, MB)
 #pragma unroll
                 for (int q = 0; q < TR / W; ++q) {
                     const int rr = warp * (TR / W) + q;
-                    tmem_cp_512b_x4((uint32_t)kr[3] + 8 * rr, stage0 + (KL + rr) * PITCH);
-                    tmem_cp_512b_x4((uint32_t)kr[3] + 8 * rr + 4, stage0 + (KL + rr) * PITCH + 512);
+                    tmem_cp_512b_x4((uint32_t)kr[3] + TCPR * rr, stage0 + (KL + rr) * PITCH);
+                    if (!BF) tmem_cp_512b_x4((uint32_t)kr[3] + TCPR * rr + 4, stage0 + (KL + rr) * PITCH + 512);
                 }
                 tmem_commit(smem_addr(&bars[4]));
             }
@@ -634,8 +640,11 @@ __global__ void __launch_bounds__(W * 32, MB)
                     if (TM && slot >= n_sm && slot < n) {
                         // Tensor-memory rows: (TMEM address, value) in the second
                         // region, from its first slot, so it reads 16 bytes at a time.
-                        reinterpret_cast<uint2*>(wl)[32 + slot - n_sm] =
-                            make_uint2(tlane + (uint32_t)(col - k0 - KL) * 8u, vb);
+                        if constexpr (BF)  // column | bf16 value << 16 (the warp's lanes added at use)
+                            reinterpret_cast<uint32_t*>(wl)[32 + slot - n_sm] = (uint32_t)(col - k0 - KL) * TCPR | (vb << 16);
+                        else
+                            reinterpret_cast<uint2*>(wl)[32 + slot - n_sm] =
+                                make_uint2(tlane + (uint32_t)(col - k0 - KL) * TCPR, vb);
                     } else if (slot < npad) {
                         const bool live = slot < n;
                         const uint32_t off = live ? (uint32_t)(col - k0) * PITCH : 0u;
@@ -744,7 +753,8 @@ __global__ void __launch_bounds__(W * 32, MB)
                             if (tm_failed) kr[2] = 1;
                             tmem_fence_after_sync();
                         }
-                        if (tm_ready && USM_TM_PIPE) {
+                        if constexpr (!BF && USM_TM_PIPE != 0) {
+                        if (tm_ready) {
                             // Pairs of entries, software-pipelined: the next pair's
                             // loads are in flight while the current pair's FMAs run
                             // (the wait covers every outstanding load, so the loads
@@ -794,6 +804,40 @@ __global__ void __launch_bounds__(W * 32, MB)
                                 fma_f32(w, e.y);
                             }
                         }
+                        }
+                        if constexpr (BF) {
+                          if (tm_ready) {
+                            // bf16: four entries (column | value << 16) a 128-bit load.
+                            const uint32_t tl = wl_addr + 32 * ENTRY;
+                            const int m = n - n_sm;
+                            auto fma_w = [&](uint4 w, uint32_t e) {
+                                const uint16_t av = hi16(e);
+                                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    acc[i][2 * q] = fma_bf16(av, lo16(ww[q]), acc[i][2 * q]);
+                                    acc[i][2 * q + 1] = fma_bf16(av, hi16(ww[q]), acc[i][2 * q + 1]);
+                                }
+                            };
+                            int t = 0;
+#pragma unroll 1
+                            for (; t + 4 <= m; t += 4) {
+                                const uint4 e = lds128(tl + t * 4);
+                                uint4 w0, w1, w2, w3;
+                                tmem_ld4x4(tlane + (e.x & 0xffffu), tlane + (e.y & 0xffffu), tlane + (e.z & 0xffffu),
+                                           tlane + (e.w & 0xffffu), w0, w1, w2, w3);
+                                fma_w(w0, e.x);
+                                fma_w(w1, e.y);
+                                fma_w(w2, e.z);
+                                fma_w(w3, e.w);
+                            }
+#pragma unroll 1
+                            for (; t < m; ++t) {
+                                const uint32_t e = lds32(tl + t * 4);
+                                fma_w(tmem_ld4(tlane + (e & 0xffffu)), e);
+                            }
+                          }
+                        } else {
                         if (tm_ready && !USM_TM_PIPE) {
                             const uint32_t tl = wl_addr + 32 * 8;  // tensor-memory entries
                             const int m = n - n_sm;
@@ -815,6 +859,7 @@ __global__ void __launch_bounds__(W * 32, MB)
                                 tmem_ld8(e.x, w);
                                 fma_f32(w, e.y);
                             }
+                        }
                         }
                     }
                     __syncwarp();
@@ -887,7 +932,7 @@ __global__ void __launch_bounds__(W * 32, MB)
         tmem_fence_before_sync();
         __syncthreads();
         tmem_fence_after_sync();
-        if (warp == 0) tmem_dealloc((uint32_t)kr[3], 512);
+        if (warp == 0) tmem_dealloc((uint32_t)kr[3], TCOLS);
     }
 
     if (kr[2]) {
