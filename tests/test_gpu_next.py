@@ -180,7 +180,7 @@ def test_row_softmax(usm):
 
 
 # (N, density, seg_rows); 1% of 1500 columns with N = 64 takes the fp32 gather kernel
-FUSED_CASES = [(64, 0.05, 0), (128, 0.1, 0), (300, 0.2, 0), (64, 0.3, 250), (64, 0.01, 0)]
+FUSED_CASES = [(64, 0.05, 0), (128, 0.1, 0), (300, 0.2, 0), (64, 0.3, 250), (64, 0.01, 0), (1300, 0.6, 0)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

@@ -179,6 +179,82 @@ def test_spmm_tensor_memory_rows(usm, schedule, M, K, N, density, seg):
     assert usm.poll_status() == 0
 
 
+# fp32 masks at least half set, N > 128, K <= 6144, with 64-row tiles x
+# 256-wide strips covering at least half the SMs: the row-group kernel.
+ROW_GROUP_CASES = [(1300, 3000, 1000, 0.6, 0), (5000, 500, 300, 0.52, 0), (2560, 2560, 300, 1.0, 1280),
+                   (2500, 6144, 300, 0.52, 0)]
+
+
+@pytest.mark.parametrize("M,K,N,density,seg", ROW_GROUP_CASES)
+def test_spmm_row_groups(usm, schedule, M, K, N, density, seg):
+    """Row groups (a staged row of B serves every row of a warp holding its
+    column): ragged strips and chunks, K under one chunk, fully dense
+    diagonal blocks (every slab reloads the windows), the largest K the
+    kernel takes, and forced schedules bit for bit; every element against
+    the oracle."""
+    if seg:
+        K = M
+        rng = np.random.default_rng([M, 154])
+        lengths = rng.binomial(seg, density, M)
+        base = (np.arange(M) // seg) * seg
+        ro, ci = W.csr_from_lengths(rng, lengths, seg, col_base=base)
+        csr = W.CSR(M, K, ro, ci, W.values_for(rng, int(ro[-1]), 1.0, "f32"), "f32", seg_rows=seg)
+    else:
+        csr = W.random_csr([M, K, N, 155], M, K, density)
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert csr.nnz >= 0.5 * M * K and 2 * ((M + 63) // 64) * ((N + 255) // 256) >= sms
+    B = W.dense(np.random.default_rng([M, K, 156]), K, N)
+    rod, cid, vd = csr_dev(csr)
+    Bd = dev(B)
+    perm = usm.row_swizzle(rod, K, seg)
+    outs = []
+    for r, t, s_ in [(0, 0, 0), (2, 0, 0), (4, 0, 0), (0, 40, 0), (4, 200, 0)]:
+        schedule(r, t, s_)
+        outs.append(host(usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=perm, seg_rows=seg)))
+    for c in outs[1:]:
+        assert np.array_equal(c, outs[0])
+    ref, S = oracle_spmm(csr, B, "f32")
+    assert_within(outs[0], ref, S, TOL["f32"], f"row-group spmm {M}x{K}x{N}")
+    assert usm.poll_status() == 0
+
+
+def test_spmm_row_groups_integer_valued_bit_exact(usm):
+    M, K, N = 1300, 1000, 1000
+    csr = W.random_csr([M, K, 157], M, K, 0.6, int_valued=True)
+    B = W.dense(np.random.default_rng(158), K, N, 1.0, "f32", int_valued=True)
+    ro, ci, vals = csr_dev(csr)
+    C = host(usm.spmm(ro, ci, vals, dev(B), K=K))
+    ref, _ = oracle_spmm(csr, B, "f32")
+    assert np.array_equal(C.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("density", [0.1, 0.6])
+def test_spmm_non_finite_b_reaches_only_its_rows(usm, density):
+    """Infinities and NaNs in B reach exactly the outputs whose rows hold
+    those columns (no product of an absent entry is formed), for the row
+    kernel (10% set) and the row-group kernel (60%), as in the oracle."""
+    M, K, N = 1300, 1500, 1000
+    csr = W.random_csr([M, K, 159], M, K, density)
+    B = W.dense(np.random.default_rng(160), K, N)
+    B[7, 3] = np.inf
+    B[700, 500] = -np.inf
+    B[1499, 999] = np.nan
+    B[3, 0:4] = [np.inf, -np.inf, np.nan, np.inf]
+    ro, ci, vals = csr_dev(csr)
+    C = host(usm.spmm(ro, ci, vals, dev(B), K=K))
+    ref = oracle.spmm(M, K, csr.row_offsets, csr.col_indices, oracle.widen(csr.values, "f32"),
+                      oracle.widen(B, "f32"))
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(C), fin)
+    assert np.array_equal(np.isnan(C), np.isnan(ref))
+    assert np.array_equal(np.sign(C[np.isinf(ref)]), np.sign(ref[np.isinf(ref)]))
+    Bf = np.where(np.isfinite(B), B, 0.0).astype(np.float32)
+    ref_f, S = oracle_spmm(csr, Bf, "f32")
+    assert_within(np.where(fin, C, 0.0), np.where(fin, ref_f, 0.0), S, TOL["f32"], "finite outputs")
+    assert (~fin).sum() > 0
+
+
 def test_spmm_long_k_fp32(usm):
     """fp32 with more than 128 chunks of K (K = 40000: 209 chunks of 192
     rows) takes the kernel with a second-level accumulator; with every

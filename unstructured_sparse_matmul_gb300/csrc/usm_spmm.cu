@@ -4,6 +4,7 @@
 
 #include "usm_internal.h"
 #include "usm_spmm_kernel.cuh"
+#include "usm_spmm_group.cuh"
 
 namespace usm {
 namespace {
@@ -15,17 +16,29 @@ namespace {
 #define USM_SPMM_VL 0
 #endif
 
-template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK, bool TM, bool SMX, bool VL>
+// UG: the row-group kernel (usm_spmm_group.cuh; fp32 256-column strips, one
+// stage, G = R row slots a warp) instead of the row kernel.
+template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK, bool TM, bool SMX, bool VL,
+          bool UG = false>
 int launch_kernel(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaStream_t stream) {
     using C_ = SpmmCfg<BF, L, VEC, R, W, KC, NS, TM, VL>;
     CUtensorMap map;
     if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::BOX_COLS, C_::BOX_ROWS)) return USM_ERR_CUDA;
-    auto kern = spmm_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK, TM, SMX, VL>;
+    auto pick = [] {
+        if constexpr (UG) {
+            static_assert(!BF && L == 32 && VEC == 8 && NS == 1 && MB == 1 && !LONGK && !TM && !VL, "row groups");
+            return spmm_group_kernel<KC, W, R, SMX>;
+        } else {
+            return spmm_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK, TM, SMX, VL>;
+        }
+    };
+    auto kern = pick();
+    constexpr int SMEM = UG ? GroupCfg<KC, W, R>::SMEM : C_::SMEM;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 31 && !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::SMEM) !=
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) !=
             cudaSuccess)
             return USM_ERR_CUDA;
         __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_ACQ_REL);
@@ -39,14 +52,17 @@ int launch_kernel(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaS
     if (tiles > 0x7fffffffLL) return USM_ERR_UNSUPPORTED;
     const dim3 grid((unsigned)tiles, (a.N + C_::NT - 1) / C_::NT);
     if (grid.y > 65535u) return USM_ERR_UNSUPPORTED;
-    kern<<<grid, C_::THREADS, C_::SMEM, stream>>>(map, a);
+    kern<<<grid, C_::THREADS, SMEM, stream>>>(map, a);
     return cudaGetLastError() == cudaSuccess ? USM_OK : USM_ERR_CUDA;
 }
 
 template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK = false, bool TM = false,
-          bool SMX = false>
+          bool SMX = false, bool UG = false>
 int launch_cfg(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaStream_t stream) {
-    if constexpr (USM_SPMM_VL && L == 32 && !TM) {
+    if constexpr (UG) {
+        return launch_kernel<BF, L, VEC, R, W, KC, NS, MB, false, false, SMX, false, true>(a, tiles_per_block, B, ldb,
+                                                                                         stream);
+    } else if constexpr (USM_SPMM_VL && L == 32 && !TM) {
         const bool aligned = (reinterpret_cast<uintptr_t>(a.col_indices) & 15u) == 0 &&
                              (reinterpret_cast<uintptr_t>(a.values) & (BF ? 7u : 15u)) == 0;
         if (aligned) return launch_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK, TM, SMX, true>(a, tiles_per_block, B, ldb, stream);
@@ -94,7 +110,7 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 // Measured against the fewest tiles: FFN SpMM 7-14% faster, LSTM 5-13%,
 // ResNet 31%, attention 6%.
 template <bool BF, int L, int VEC, int W, int KC, int NS, int MB, int RA = 2, int RB = 4, bool TM = false,
-          bool SMX = false>
+          bool SMX = false, bool UG = false>
 int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) {
     const int sms = sm_count_current_device();
     const long long slots = (long long)sms * MB;
@@ -128,18 +144,20 @@ int launch_pick(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream) 
     // RB at equal tile counts, never slower).
     int R = cost(ta) < cost(tb) ? RA : RB, T = R == RA ? ta : tb;
     if (R == RB && (long long)tb * RA * W >= a.seg_rows) R = RA;
+    // Row groups: RB slots a warp share each staged row among more rows.
+    if (UG) R = RB, T = tb;
     if (ov.rows_per_warp == RA) R = RA, T = ta;
     else if (ov.rows_per_warp == RB) R = RB, T = tb;
     else if (ov.rows_per_warp != 0) return USM_ERR_UNSUPPORTED;
     // fp32 with more than 128 chunks of K: the kernel with a second-level
     // accumulator keeps the worst-case rounding bound (RA rows a warp only,
     // for the registers it takes).
-    if (!BF && (a.K + KC - 1) / KC > 128) {
+    if (!UG && !BF && (a.K + KC - 1) / KC > 128) {
         if (ov.rows_per_warp == RB) return USM_ERR_UNSUPPORTED;
         return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB, true, TM, SMX>(a, ta, B, ldb, stream);
     }
-    if (R == RA) return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB, false, TM, SMX>(a, T, B, ldb, stream);
-    return launch_cfg<BF, L, VEC, RB, W, KC, NS, MB, false, TM, SMX>(a, T, B, ldb, stream);
+    if (R == RA) return launch_cfg<BF, L, VEC, RA, W, KC, NS, MB, false, TM, SMX, UG>(a, T, B, ldb, stream);
+    return launch_cfg<BF, L, VEC, RB, W, KC, NS, MB, false, TM, SMX, UG>(a, T, B, ldb, stream);
 }
 
 // The six tile shapes by element type and N.  SMX: the values are the rows'
@@ -211,6 +229,25 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #ifndef USM_TM_KC
 #define USM_TM_KC (96 * F)
 #endif
+        // fp32 masks at least half set: row groups (usm_spmm_group.cuh), where
+        // a staged row of B serves all of a warp's rows holding its column.
+        // Measured against the row kernel (N = 2048, one stream): 1024x4096
+        // at 50% density 4% faster, 60% 15%, 80% 40%; 4096x1024 at 60% 16%;
+        // 30-40% density 5-17% slower (the predicated FMAs of the rows without
+        // a column cost more than the loads saved), and so are grids whose
+        // 64-row tiles cover under half the SMs (2048x2048, N = 512: 26% slower).
+        // K ≤ 6144 keeps its rounding bound.  The choice depends on M, N, K,
+        // nnz only, never on the schedule arguments.
+#ifndef USM_SPMM_GROUP
+#define USM_SPMM_GROUP 1
+#endif
+#ifndef USM_GROUP_MIN_PCT
+#define USM_GROUP_MIN_PCT 50
+#endif
+        const long long group_ctas = (long long)((a.M + 63) / 64) * ((a.N + 255) / 256);
+        if (USM_SPMM_GROUP && NS == 1 && a.K <= 6144 && 100LL * a.nnz >= (long long)USM_GROUP_MIN_PCT * cells &&
+            2 * group_ctas >= sm_count_current_device())
+            return launch_pick<false, 32, 8, W, 192, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
         if (!SMX && USM_SPMM_TMEM && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
             return launch_pick<false, 32, 8, W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
         if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
