@@ -92,11 +92,14 @@ WORKLOADS = {
     "attention_unfused": "sparse attention, 8 heads x 4096, bf16: SDDMM scores, row softmax to bf16, SpMM with V "
                          "(three calls)",
     "lstm": "LSTM-sized sweep, fp32: A 8192x4096 at 50/60/70/80/90/95/98%, B 4096x128, SpMM only",
+    "ffn_dense": "FFN shapes with denser masks, fp32: A 4096x1024 and 1024x4096 at 20/30/40/50% sparsity, "
+                 "B Kx2048, SpMM only (masks at least half set run the row-group kernel)",
     "resnet": "ResNet-50-like 1x1 conv, fp32: A 512x2048 at 80%, B 2048x3136 SpMM and SDDMM weight-gradient "
               "(X 512x3136, Y 2048x3136); L2 flushed before every step",
     "tiny": "tiny parity config, fp32: A 256x256 at 90%, B/X/Y 256x64, SpMM and SDDMM; launch-bound, so each "
             "call is timed as a CUDA graph of 100 calls (warm L2: the whole problem is 0.2 MB)",
 }
+FFN_DENSE_SPARSITIES = (20, 30, 40, 50)
 GRAPH_CALLS = 100  # calls per CUDA graph for the launch-bound workloads
 GRAPHED = {"tiny"}
 # Workloads whose operands fit in L2: a 256 MB buffer is written before every
@@ -116,6 +119,9 @@ def problems(only=None, workload="ffn"):
         return [p for p in [W.resnet()] if keep(p)]
     if workload == "tiny":
         return [W.tiny()]
+    if workload == "ffn_dense":
+        return [W.ffn(M, K, s, "f32", N=N_FFN, with_sddmm=False) for (M, K) in W.FFN_SHAPES
+                for s in FFN_DENSE_SPARSITIES if not only or only.split(":")[-1] in tag_of("f32", M, K, s)]
     out = []
     for dtype in ("f32", "bf16"):
         for (M, K) in W.FFN_SHAPES:
@@ -137,7 +143,7 @@ def ops_of(only, workload="ffn"):
         return ("sddmm", "spmm_softmax")
     if workload == "attention_unfused":
         return ("sddmm", "softmax", "spmm")
-    if workload == "lstm":
+    if workload in ("lstm", "ffn_dense"):
         return ("spmm",)
     return ("spmm", "sddmm")
 
@@ -545,7 +551,8 @@ def run_ours(args, rank, world, local_rank):
 # grid decides how often staged tiles are re-read, so a launch-model change
 # retires a capture as surely as a kernel change).
 KERNEL_SOURCES = {
-    "spmm": ("usm_spmm_kernel.cuh", "usm_spmm.cu", "usm_device.cuh", "usm_args.h", "usm_internal.h"),
+    "spmm": ("usm_spmm_kernel.cuh", "usm_spmm_group.cuh", "usm_spmm.cu", "usm_device.cuh", "usm_args.h",
+             "usm_internal.h"),
     "sddmm": ("usm_sddmm_kernel.cuh", "usm_sddmm.cu", "usm_device.cuh", "usm_args.h", "usm_internal.h"),
 }
 

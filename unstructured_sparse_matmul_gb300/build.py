@@ -3,6 +3,11 @@
 Each .cu file in csrc/ is compiled in parallel to an object, then linked into
 unstructured_sparse_matmul_gb300/_build/libusm.so.  Run as a module or call
 build_library().
+
+USM_NVCC_FLAGS (environment) adds compiler flags, e.g. the -D switches of the
+launch code's build-time options (USM_SPMM_GROUP=0 keeps fp32 SpMM on the row
+kernel); the up-to-date check looks at file times only, so rebuild with
+--force when the flags change.
 """
 from __future__ import annotations
 
@@ -50,6 +55,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     common = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                      "--expt-relaxed-constexpr"]
+    common += os.environ.get("USM_NVCC_FLAGS", "").split()
     if verbose:
         common += ["-Xptxas", "-v"]
 
