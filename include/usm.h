@@ -107,7 +107,9 @@ int csr_spmm(int M, int K, int N, int nnz,
  *   row_swizzle, seg_rows : as csr_spmm (schedule only).
  *   workspace : device scratch of at least
  *          csr_sddmm_workspace_bytes(M, K, D, nnz, in_dtype) bytes; may be
- *          NULL when that size is 0.  Its contents on entry are ignored.
+ *          NULL when that size is 0.  Its contents on entry are ignored and
+ *          undefined on return (partials already summed are dropped from the
+ *          L2 cache without being written back).
  * Limits: as csr_spmm.  nnz = 0 or M = 0 is a no-op; D = 0 zero-fills out.
  */
 size_t csr_sddmm_workspace_bytes(int M, int K, int D, int nnz, usm_dtype in_dtype);
@@ -148,8 +150,8 @@ int csr_sddmm(int M, int K, int D, int nnz,
  *          the set-up again.
  *   Allocation: none on later calls (no cudaMalloc, cudaFree or allocating
  *          library routine).
- *   Sharing: every call on a device uses the same array, which keeps the
- *          last call's contents.  On a CSR that meets the contract nothing in
+ *   Sharing: every call on a device uses the same array, whose contents
+ *          between calls are undefined.  On a CSR that meets the contract nothing in
  *          it needs to start at zero; on one that does not (see
  *          csr_validate), or after USM_ERR_TIMEOUT, the output may hold values
  *          left there by an earlier call.  Calls whose executions overlap on

@@ -61,14 +61,14 @@ def test_workspace_sizes(lib):
     assert lib.row_swizzle_workspace_bytes(4096, 1024) == 4096 * 4 + 256 * 2 * 4
     assert lib.csr_sddmm_workspace_bytes(10, 10, 64, 100, usm.USM_F32) == 0        # one strip
     assert lib.csr_sddmm_workspace_bytes(10, 10, 128, 100, usm.USM_F32) == 0
-    assert lib.csr_sddmm_workspace_bytes(100, 10, 129, 100, usm.USM_F32) == 2 * 100 * 4  # 128-wide strips
+    assert lib.csr_sddmm_workspace_bytes(100, 10, 129, 100, usm.USM_F32) == 2 * 128 * 4  # 128-wide strips
     # masks at least a quarter full use 256-wide strips (bf16 too, unless D <= 64)
     assert lib.csr_sddmm_workspace_bytes(10, 10, 129, 100, usm.USM_F32) == 0
-    assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 25, usm.USM_F32) == 2 * 28 * 4  # strips 4-aligned
-    assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 24, usm.USM_F32) == 3 * 24 * 4
-    assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 100, usm.USM_BF16) == 2 * 100 * 4
-    assert lib.csr_sddmm_workspace_bytes(100, 10, 257, 100, usm.USM_BF16) == 3 * 100 * 4
-    assert lib.csr_sddmm_workspace_bytes(10, 10, 2048, 7, usm.USM_BF16) == 16 * 8 * 4
+    assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 25, usm.USM_F32) == 2 * 32 * 4  # strips 32-aligned
+    assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 24, usm.USM_F32) == 3 * 32 * 4
+    assert lib.csr_sddmm_workspace_bytes(10, 10, 257, 100, usm.USM_BF16) == 2 * 128 * 4
+    assert lib.csr_sddmm_workspace_bytes(100, 10, 257, 100, usm.USM_BF16) == 3 * 128 * 4
+    assert lib.csr_sddmm_workspace_bytes(10, 10, 2048, 7, usm.USM_BF16) == 16 * 32 * 4
     assert lib.csr_sddmm_workspace_bytes(10, 10, 64, 7, usm.USM_BF16) == 0
     assert lib.csr_sddmm_workspace_bytes(10, 10, 0, 7, usm.USM_F32) == 0
     # general SDDMM: transposed-Y region (K x ld, 256-byte aligned) + strip partials

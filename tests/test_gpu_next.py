@@ -123,7 +123,7 @@ def test_sddmm_general_matches_specialised_form(usm):
 def test_sddmm_strip_sum_paths(usm, dtype, scale, nnz_mod4):
     """D = 300 spans several column strips, whose partials a second kernel
     adds: four nonzeros at a time when every array is aligned (strips of
-    partials are padded to a multiple of 4; with nnz % 4 = 3 the last group
+    partials are padded to a multiple of 32; with nnz % 4 = 3 the last group
     is ragged), else one at a time (an output starting one element into its
     buffer forces that).  Both add the same terms in the same order."""
     import torch

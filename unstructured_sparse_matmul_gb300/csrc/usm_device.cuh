@@ -237,6 +237,12 @@ __device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float c) {
 __device__ __forceinline__ uint16_t lo16(uint32_t w) { return static_cast<uint16_t>(w); }
 __device__ __forceinline__ uint16_t hi16(uint32_t w) { return static_cast<uint16_t>(w >> 16); }
 
+// Drop the 128-byte line at p (128-byte aligned) from L2 without writing it
+// back: its contents become undefined.  For scratch data that is dead.
+__device__ __forceinline__ void l2_discard_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Shared-memory loads by 32-bit shared address.  volatile keeps them after
 // the barrier waits that publish the data they read.
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

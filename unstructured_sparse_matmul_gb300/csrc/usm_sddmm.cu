@@ -32,7 +32,9 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
     if (nstrips > 65535) return USM_ERR_UNSUPPORTED;
     void* final_out = a.out;
     // Strips of partials lie partial_stride(nnz) elements apart (a multiple of
-    // 4, so every strip starts 16-byte aligned for the strip sum's loads).
+    // 32: every strip starts 16-byte aligned for the strip sum's loads, and
+    // 128-byte aligned when the workspace is, so no 128-byte line of partials
+    // spans two strips).
     const long long stride = partial_stride(a.nnz);
     if (nstrips > 1) {
         if (ws == nullptr || ws_bytes < (size_t)nstrips * (size_t)stride * sizeof(float))
@@ -114,10 +116,11 @@ int launch_cfg(SddmmArgs a, const void* Y, int ldy, void* ws, size_t ws_bytes, c
         const long long items = vec ? (a.nnz + 3) / 4 : a.nnz;
         long long blocks = (items + 255) / 256;
         if (blocks > 8 * sms) blocks = 8 * sms;
+        const int discard = USM_PARTIAL_DISCARD && (uintptr_t)ws % 128 == 0;
         if (vec)
             sddmm_strip_sum4_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz, stride,
                                                                      nstrips, final_out, a.out_bf16, a.scale,
-                                                                     a.scale_bf16);
+                                                                     a.scale_bf16, discard);
         else
             sddmm_strip_sum_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const float*>(ws), a.nnz, stride,
                                                                     nstrips, final_out, a.out_bf16, a.scale,
@@ -141,7 +144,7 @@ int strip_width(int M, int K, int D, int nnz, bool bf16) {
 
 }  // namespace
 
-long long partial_stride(long long nnz) { return (nnz + 3) / 4 * 4; }
+long long partial_stride(long long nnz) { return (nnz + 31) / 32 * 32; }
 
 size_t sddmm_workspace_bytes(int M, int K, int D, int nnz, bool bf16) {
     if (D <= 0 || nnz <= 0) return 0;
