@@ -92,14 +92,16 @@ WORKLOADS = {
     "attention_unfused": "sparse attention, 8 heads x 4096, bf16: SDDMM scores, row softmax to bf16, SpMM with V "
                          "(three calls)",
     "lstm": "LSTM-sized sweep, fp32: A 8192x4096 at 50/60/70/80/90/95/98%, B 4096x128, SpMM only",
-    "ffn_dense": "FFN shapes with denser masks, fp32: A 4096x1024 and 1024x4096 at 20/30/40/50% sparsity, "
-                 "B Kx2048, SpMM only (masks at least half set run the row-group kernel)",
+    "dense_masks": "denser masks, fp32 SpMM only: the FFN shapes (A 4096x1024 and 1024x4096, B Kx2048) at "
+                   "20/30/40/50% sparsity and the LSTM shape (A 8192x4096, B 4096x128) at 10/20/30/40% (masks at "
+                   "least half set, or 55% with N <= 128, run the row-group kernel)",
     "resnet": "ResNet-50-like 1x1 conv, fp32: A 512x2048 at 80%, B 2048x3136 SpMM and SDDMM weight-gradient "
               "(X 512x3136, Y 2048x3136); L2 flushed before every step",
     "tiny": "tiny parity config, fp32: A 256x256 at 90%, B/X/Y 256x64, SpMM and SDDMM; launch-bound, so each "
             "call is timed as a CUDA graph of 100 calls (warm L2: the whole problem is 0.2 MB)",
 }
-FFN_DENSE_SPARSITIES = (20, 30, 40, 50)
+DENSE_FFN_SPARSITIES = (20, 30, 40, 50)
+DENSE_LSTM_SPARSITIES = (10, 20, 30, 40)
 GRAPH_CALLS = 100  # calls per CUDA graph for the launch-bound workloads
 GRAPHED = {"tiny"}
 # Workloads whose operands fit in L2: a 256 MB buffer is written before every
@@ -119,9 +121,12 @@ def problems(only=None, workload="ffn"):
         return [p for p in [W.resnet()] if keep(p)]
     if workload == "tiny":
         return [W.tiny()]
-    if workload == "ffn_dense":
-        return [W.ffn(M, K, s, "f32", N=N_FFN, with_sddmm=False) for (M, K) in W.FFN_SHAPES
-                for s in FFN_DENSE_SPARSITIES if not only or only.split(":")[-1] in tag_of("f32", M, K, s)]
+    if workload == "dense_masks":
+        ffn = [W.ffn(M, K, s, "f32", N=N_FFN, with_sddmm=False) for (M, K) in W.FFN_SHAPES
+               for s in DENSE_FFN_SPARSITIES if not only or only.split(":")[-1] in tag_of("f32", M, K, s)]
+        lstm = [W.lstm(s) for s in DENSE_LSTM_SPARSITIES
+                if not only or only.split(":")[-1] in tag_of("f32", 8192, 4096, s)]
+        return ffn + lstm
     out = []
     for dtype in ("f32", "bf16"):
         for (M, K) in W.FFN_SHAPES:
@@ -143,7 +148,7 @@ def ops_of(only, workload="ffn"):
         return ("sddmm", "spmm_softmax")
     if workload == "attention_unfused":
         return ("sddmm", "softmax", "spmm")
-    if workload in ("lstm", "ffn_dense"):
+    if workload in ("lstm", "dense_masks"):
         return ("spmm",)
     return ("spmm", "sddmm")
 

@@ -179,19 +179,21 @@ def test_spmm_tensor_memory_rows(usm, schedule, M, K, N, density, seg):
     assert usm.poll_status() == 0
 
 
-# fp32 masks at least half set, N > 128, K <= 6144, with 64-row tiles x
-# 256-wide strips covering at least half the SMs: the row-group kernel.
+# fp32 masks at least half set (N > 128, 256-wide strips) or 55% set
+# (64 < N <= 128, 128-wide strips), K <= 6144, with 64-row tiles x strips
+# covering at least half the SMs: the row-group kernel.
 ROW_GROUP_CASES = [(1300, 3000, 1000, 0.6, 0), (5000, 500, 300, 0.52, 0), (2560, 2560, 300, 1.0, 1280),
-                   (2500, 6144, 300, 0.52, 0)]
+                   (2500, 6144, 300, 0.52, 0), (5000, 1000, 100, 0.6, 0), (5000, 2500, 128, 0.58, 0),
+                   (5000, 1500, 65, 0.9, 0)]
 
 
 @pytest.mark.parametrize("M,K,N,density,seg", ROW_GROUP_CASES)
 def test_spmm_row_groups(usm, schedule, M, K, N, density, seg):
     """Row groups (a staged row of B serves every row of a warp holding its
-    column): ragged strips and chunks, K under one chunk, fully dense
-    diagonal blocks (every slab reloads the windows), the largest K the
-    kernel takes, and forced schedules bit for bit; every element against
-    the oracle."""
+    column), on 256- and 128-wide strips: ragged strips and chunks, K under
+    one chunk, fully dense diagonal blocks (every slab reloads the windows),
+    the largest K the kernel takes, and forced schedules bit for bit; every
+    element against the oracle."""
     if seg:
         K = M
         rng = np.random.default_rng([M, 154])
@@ -203,7 +205,9 @@ def test_spmm_row_groups(usm, schedule, M, K, N, density, seg):
         csr = W.random_csr([M, K, N, 155], M, K, density)
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert csr.nnz >= 0.5 * M * K and 2 * ((M + 63) // 64) * ((N + 255) // 256) >= sms
+    strip = 256 if N > 128 else 128
+    assert csr.nnz >= (0.5 if N > 128 else 0.55) * M * K
+    assert 2 * ((M + 63) // 64) * ((N + strip - 1) // strip) >= sms
     B = W.dense(np.random.default_rng([M, K, 156]), K, N)
     rod, cid, vd = csr_dev(csr)
     Bd = dev(B)

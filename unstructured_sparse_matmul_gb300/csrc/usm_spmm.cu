@@ -16,8 +16,8 @@ namespace {
 #define USM_SPMM_VL 0
 #endif
 
-// UG: the row-group kernel (usm_spmm_group.cuh; fp32 256-column strips, one
-// stage, G = R row slots a warp) instead of the row kernel.
+// UG: the row-group kernel (usm_spmm_group.cuh; fp32 128- or 256-column
+// strips, one stage, G = R row slots a warp) instead of the row kernel.
 template <bool BF, int L, int VEC, int R, int W, int KC, int NS, int MB, bool LONGK, bool TM, bool SMX, bool VL,
           bool UG = false>
 int launch_kernel(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaStream_t stream) {
@@ -26,14 +26,15 @@ int launch_kernel(SpmmArgs a, int tiles_per_block, const void* B, int ldb, cudaS
     if (!encode_tensor_map_2d(&map, B, BF, a.K, a.N, ldb, C_::BOX_COLS, C_::BOX_ROWS)) return USM_ERR_CUDA;
     auto pick = [] {
         if constexpr (UG) {
-            static_assert(!BF && L == 32 && VEC == 8 && NS == 1 && MB == 1 && !LONGK && !TM && !VL, "row groups");
-            return spmm_group_kernel<KC, W, R, SMX>;
+            static_assert(!BF && L == 32 && (VEC == 4 || VEC == 8) && NS == 1 && MB == 1 && !LONGK && !TM && !VL,
+                          "row groups");
+            return spmm_group_kernel<KC, W, R, VEC, SMX>;
         } else {
             return spmm_kernel<BF, L, VEC, R, W, KC, NS, MB, LONGK, TM, SMX, VL>;
         }
     };
     auto kern = pick();
-    constexpr int SMEM = UG ? GroupCfg<KC, W, R>::SMEM : C_::SMEM;
+    constexpr int SMEM = UG ? GroupCfg<KC, W, R, VEC>::SMEM : C_::SMEM;
     static int configured_mask = 0;  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -208,7 +209,36 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         // at the same registers.  Measured against 256-wide strips with up to 4
         // rows a warp: FFN 95% 6-11% faster, 90% -2..+3%, LSTM even.
         const bool sparse = 100LL * a.nnz < (long long)USM_SPMM_HS_PCT * cells;
+        // fp32 masks at least half set: row groups (usm_spmm_group.cuh), where
+        // a staged row of B serves all of a warp's rows holding its column.
+        // Measured against the row kernel (N = 2048, one stream): 1024x4096
+        // at 50% density 4% faster, 60% 15%, 80% 40%; 4096x1024 at 60% 16%;
+        // 30-40% density 5-17% slower (the predicated FMAs of the rows without
+        // a column cost more than the loads saved), and so are grids whose
+        // 64-row tiles cover under half the SMs (2048x2048, N = 512: 26% slower).
+        // 64 < N <= 128 takes 128-column strips, where each column carries half
+        // the FMAs for the same list work: 8192x4096, N = 128, 50% density even,
+        // 60% 13% faster, 70% 28%, 90% 54%; 40% density 9% slower; so from
+        // 55% there.  K <= 6144 keeps its rounding bound.  The choice depends
+        // on M, N, K, nnz only, never on the schedule arguments.
+#ifndef USM_SPMM_GROUP
+#define USM_SPMM_GROUP 1
+#endif
+#ifndef USM_GROUP_MIN_PCT
+#define USM_GROUP_MIN_PCT 50
+#endif
+#ifndef USM_GROUP_MIN_PCT_N128
+#define USM_GROUP_MIN_PCT_N128 55
+#endif
+        auto groups = [&](int strip) {
+            const long long ctas = (long long)((a.M + 63) / 64) * ((a.N + strip - 1) / strip);
+            const long long pct = strip == 128 ? USM_GROUP_MIN_PCT_N128 : USM_GROUP_MIN_PCT;
+            return USM_SPMM_GROUP && NS == 1 && a.K <= 6144 && 100LL * a.nnz >= pct * cells &&
+                   2 * ctas >= sm_count_current_device();
+        };
         if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
+        if (a.N <= 128 && groups(128))
+            return launch_pick<false, 32, 4, W, 384, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
         if (a.N <= 128) {
             if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
             return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
@@ -229,25 +259,7 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #ifndef USM_TM_KC
 #define USM_TM_KC (96 * F)
 #endif
-        // fp32 masks at least half set: row groups (usm_spmm_group.cuh), where
-        // a staged row of B serves all of a warp's rows holding its column.
-        // Measured against the row kernel (N = 2048, one stream): 1024x4096
-        // at 50% density 4% faster, 60% 15%, 80% 40%; 4096x1024 at 60% 16%;
-        // 30-40% density 5-17% slower (the predicated FMAs of the rows without
-        // a column cost more than the loads saved), and so are grids whose
-        // 64-row tiles cover under half the SMs (2048x2048, N = 512: 26% slower).
-        // K ≤ 6144 keeps its rounding bound.  The choice depends on M, N, K,
-        // nnz only, never on the schedule arguments.
-#ifndef USM_SPMM_GROUP
-#define USM_SPMM_GROUP 1
-#endif
-#ifndef USM_GROUP_MIN_PCT
-#define USM_GROUP_MIN_PCT 50
-#endif
-        const long long group_ctas = (long long)((a.M + 63) / 64) * ((a.N + 255) / 256);
-        if (USM_SPMM_GROUP && NS == 1 && a.K <= 6144 && 100LL * a.nnz >= (long long)USM_GROUP_MIN_PCT * cells &&
-            2 * group_ctas >= sm_count_current_device())
-            return launch_pick<false, 32, 8, W, 192, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
+        if (groups(256)) return launch_pick<false, 32, 8, W, 192, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
         if (!SMX && USM_SPMM_TMEM && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
             return launch_pick<false, 32, 8, W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
         if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);

@@ -46,9 +46,9 @@
 namespace usm {
 namespace {
 
-template <int KC, int W, int G>
+template <int KC, int W, int G, int VEC = 8>
 struct GroupCfg {
-    using Base = SpmmCfg<false, 32, 8, G, W, KC, 1>;
+    using Base = SpmmCfg<false, 32, VEC, G, W, KC, 1>;
     // A warp's list for one slab: 33 column headers (the last one empty, so
     // the walk may load one column ahead) and 33 x G values.
     static constexpr int HDR_BYTES = 144;
@@ -57,11 +57,12 @@ struct GroupCfg {
     static constexpr int SLABS = KC / 32;
 };
 
-// c += x·w for the 8 fp32 of a lane (packed FMAs).
-__device__ __forceinline__ void fma8(float (&c)[8], const uint32_t (&w)[8], float x) {
+// c += x·w for the VEC fp32 of a lane (packed FMAs).
+template <int VEC>
+__device__ __forceinline__ void fma_vec(float (&c)[VEC], const uint32_t (&w)[VEC], float x) {
     const float2 a2 = make_float2(x, x);
 #pragma unroll
-    for (int q = 0; q < 8; q += 2) {
+    for (int q = 0; q < VEC; q += 2) {
         float2 c2 = make_float2(c[q], c[q + 1]);
         c2 = __ffma2_rn(a2, make_float2(__uint_as_float(w[q]), __uint_as_float(w[q + 1])), c2);
         c[q] = c2.x;
@@ -69,15 +70,18 @@ __device__ __forceinline__ void fma8(float (&c)[8], const uint32_t (&w)[8], floa
     }
 }
 
-template <int KC, int W, int G, bool SMX = false>
+// VEC = 8: 256-column strips (two 16-byte loads a column); VEC = 4:
+// 128-column strips (one).
+template <int KC, int W, int G, int VEC = 8, bool SMX = false>
 __global__ void __launch_bounds__(W * 32, 1)
     spmm_group_kernel(const __grid_constant__ CUtensorMap tmB, const SpmmArgs a) {
-    using GC = GroupCfg<KC, W, G>;
+    using GC = GroupCfg<KC, W, G, VEC>;
     using C_ = typename GC::Base;
-    constexpr int PITCH = C_::PITCH, STAGE = C_::STAGE, VEC = 8;
+    constexpr int PITCH = C_::PITCH, STAGE = C_::STAGE, NCH = C_::NCH;
     constexpr int FOLD = 2;  // slabs summed in a partial before it joins the row total
-    static_assert(KC % 32 == 0 && C_::NBOX == 1 && PITCH == 1024 && (G == 2 || G == 4 || G == 8),
-                  "256-column fp32 strips, slabs of 32 rows, 2, 4 or 8 row slots a warp");
+    static_assert(KC % 32 == 0 && C_::NBOX == 1 && (VEC == 4 || VEC == 8) && PITCH == 128 * VEC &&
+                      (G == 2 || G == 4 || G == 8),
+                  "128- or 256-column fp32 strips, slabs of 32 rows, 2, 4 or 8 row slots a warp");
 
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGE);  // [0] TMA
@@ -266,15 +270,17 @@ __global__ void __launch_bounds__(W * 32, 1)
                 }
                 __syncwarp();
 
-                // One column: the lane's 8 fp32 of its staged row, times each
+                // One column: the lane's VEC fp32 of its staged row, times each
                 // holding slot's value, into that slot's partial (predicated
                 // on the slot mask: slots without the column do no FMA).
-                auto load_col = [&](int u, uint32_t& h, uint32_t (&w)[8], uint32_t (&x)[G]) {
+                auto load_col = [&](int u, uint32_t& h, uint32_t (&w)[VEC], uint32_t (&x)[G]) {
                     h = lds32(hdr_addr + 4 * u);
                     const uint32_t off = h & ~(uint32_t)(PITCH - 1);
-                    const uint4 b0 = lds128(stage + off), b1 = lds128(stage + off + 512);
-                    w[0] = b0.x; w[1] = b0.y; w[2] = b0.z; w[3] = b0.w;
-                    w[4] = b1.x; w[5] = b1.y; w[6] = b1.z; w[7] = b1.w;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        const uint4 b = lds128(stage + off + C_::piece_off(c));
+                        w[4 * c] = b.x; w[4 * c + 1] = b.y; w[4 * c + 2] = b.z; w[4 * c + 3] = b.w;
+                    }
                     if constexpr (G == 2) {
                         const uint2 q = lds64(val_addr + u * 8);
                         x[0] = q.x;
@@ -287,15 +293,15 @@ __global__ void __launch_bounds__(W * 32, 1)
                         }
                     }
                 };
-                auto fma_col = [&](uint32_t h, const uint32_t (&w)[8], const uint32_t (&x)[G]) {
+                auto fma_col = [&](uint32_t h, const uint32_t (&w)[VEC], const uint32_t (&x)[G]) {
 #pragma unroll
                     for (int i = 0; i < G; ++i)
-                        if (h & (1u << i)) fma8(cs[i], w, __uint_as_float(x[i]));
+                        if (h & (1u << i)) fma_vec<VEC>(cs[i], w, __uint_as_float(x[i]));
                 };
                 // Software-pipelined: column u + 1 (or the empty header past
                 // the last, whose mask does nothing) loads while column u's
                 // FMAs run.
-                uint32_t h0, h1, w0[8], w1[8], x0[G], x1[G];
+                uint32_t h0, h1, w0[VEC], w1[VEC], x0[G], x1[G];
                 if (ucols > 0) load_col(0, h0, w0, x0);
 #pragma unroll 1
                 for (int u = 0; u < ucols; u += 2) {
