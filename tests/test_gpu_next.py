@@ -231,6 +231,32 @@ def test_spmm_row_softmax_matches_unfused_chain(usm, dtype, N, density, seg, swz
     assert_within(fused, ref, S, tol, f"fused softmax spmm {dtype} N={N}")
 
 
+@pytest.mark.parametrize("N", [100, 600])
+def test_spmm_row_softmax_row_groups(usm, N):
+    """fp32 scores on masks 60% set with enough rows for the row-group kernel
+    (128-wide strips for N = 100, 256-wide for N = 600): the fused call gives
+    the unfused chain's bits and the oracle chain's result."""
+    import torch
+    M, K = 5000, 700
+    csr = W.random_csr([N, 23], M, K, 0.6)
+    rng = np.random.default_rng([N, 24])
+    s = (rng.standard_normal(csr.nnz) * 3).astype(np.float32)
+    B = W.dense(rng, K, N)
+    ro, ci = dev(csr.row_offsets), dev(csr.col_indices)
+    perm = usm.row_swizzle(ro, K)
+    Bd, sd = dev(B), dev(s)
+    fused = host(usm.spmm_row_softmax(ro, ci, sd, Bd, K=K, row_swizzle=perm))
+    P = usm.row_softmax(ro, sd, out_dtype=torch.float32)
+    unfused = host(usm.spmm(ro, ci, P, Bd, K=K, row_swizzle=perm))
+    assert np.array_equal(fused, unfused)
+    assert usm.poll_status() == 0
+    p64 = oracle.csr_softmax(csr.row_offsets, s.astype(np.float64))
+    Bw = oracle.widen(B, "f32")
+    ref = oracle.spmm(M, K, csr.row_offsets, csr.col_indices, p64, Bw)
+    S = oracle.spmm_error_scale(M, K, csr.row_offsets, csr.col_indices, p64, Bw)
+    assert_within(fused, ref, S, 2e-5, f"row-group fused softmax spmm N={N}")
+
+
 @pytest.mark.slow
 def test_attention_chain_with_softmax(usm):
     import torch
