@@ -189,9 +189,9 @@ int launch_gather(const SpmmArgs& a, const void* B, int ldb, cudaStream_t stream
 template <bool SMX>
 int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SPMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
-    // Every kernel choice below depends on the problem (nnz over M·K, N, the
-    // element type), never on the schedule arguments (swizzle, seg_rows), so
-    // those never change the result.
+    // Every kernel choice below depends on the problem (M, N, K, nnz, the
+    // element type, the device's SM count), never on the schedule arguments
+    // (swizzle, seg_rows), so those never change the result.
     const long long cells = (long long)a.M * a.K;
     {
         const ScheduleOverride ov = schedule_override();
