@@ -233,6 +233,23 @@ def test_spmm_row_groups_integer_valued_bit_exact(usm):
     assert np.array_equal(C.astype(np.float64), ref)
 
 
+@pytest.mark.parametrize("N,ldb,ldc", [(300, 312, 304), (100, 132, 104)])
+def test_spmm_row_groups_leading_dimensions(usm, N, ldb, ldc):
+    """Row groups (256- and 128-wide strips) on B and C that are views of
+    wider buffers: the right result, and nothing written past column N."""
+    import torch
+    M, K = 5000, 700
+    csr = W.random_csr([N, 161], M, K, 0.6)
+    Bbig = W.dense(np.random.default_rng([N, 162]), K, ldb)
+    out = torch.zeros((M, ldc), device="cuda")
+    ro, ci, vals = csr_dev(csr)
+    usm.spmm(ro, ci, vals, dev(Bbig)[:, :N], K=K, out=out[:, :N])
+    ref, S = oracle_spmm(csr, np.ascontiguousarray(Bbig[:, :N]), "f32")
+    C = host(out)
+    assert_within(C[:, :N], ref, S, TOL["f32"], f"row-group ld N={N}")
+    assert np.all(C[:, N:] == 0), "wrote outside the N columns"
+
+
 @pytest.mark.parametrize("density", [0.1, 0.6])
 def test_spmm_non_finite_b_reaches_only_its_rows(usm, density):
     """Infinities and NaNs in B reach exactly the outputs whose rows hold
