@@ -223,6 +223,31 @@ def test_spmm_row_groups(usm, schedule, M, K, N, density, seg):
     assert usm.poll_status() == 0
 
 
+@pytest.mark.parametrize("N", [100, 300])
+def test_spmm_row_groups_schedule_arguments_do_not_change_bits(usm, N):
+    """Two fully dense diagonal blocks (the mask half set, so 256-wide row
+    groups; 128-wide ones start at 55%, so N = 100 takes the row kernel):
+    no swizzle, a global swizzle, and per-block swizzles with and without
+    seg_rows give the same bits."""
+    seg = 1280
+    M = K = 2 * seg
+    rng = np.random.default_rng([N, 163])
+    lengths = np.full(M, seg)
+    base = (np.arange(M) // seg) * seg
+    ro, ci = W.csr_from_lengths(rng, lengths, seg, col_base=base)
+    csr = W.CSR(M, K, ro, ci, W.values_for(rng, int(ro[-1]), 1.0, "f32"), "f32", seg_rows=seg)
+    B = W.dense(rng, K, N)
+    rod, cid, vd = csr_dev(csr)
+    Bd = dev(B)
+    variants = [(None, 0), (usm.row_swizzle(rod, K), 0), (usm.row_swizzle(rod, K, seg), seg),
+                (usm.row_swizzle(rod, K, seg), 0)]
+    Cs = [host(usm.spmm(rod, cid, vd, Bd, K=K, row_swizzle=p, seg_rows=sr)) for p, sr in variants]
+    for c in Cs[1:]:
+        assert np.array_equal(c, Cs[0])
+    ref, S = oracle_spmm(csr, B, "f32")
+    assert_within(Cs[0], ref, S, TOL["f32"], f"two dense blocks N={N}")
+
+
 def test_spmm_row_groups_integer_valued_bit_exact(usm):
     M, K, N = 1300, 1000, 1000
     csr = W.random_csr([M, K, 157], M, K, 0.6, int_valued=True)
