@@ -252,8 +252,9 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #ifndef USM_TM_RB
 #define USM_TM_RB 4
 #endif
-        // fp32 256-wide strips of masks at least a quarter set: the last 64
-        // rows of every chunk also go to tensor memory (measured on the FFN
+        // fp32 256-wide strips of masks at least a quarter set (that row
+        // groups did not take above): the last 64 rows of every chunk also go
+        // to tensor memory (measured on the FFN
         // launches at 70% sparsity: 5-9% faster; at 80% even; 10-20% slower at
         // 90-95%, where the copies and their waits are not paid back).
 #ifndef USM_TM_KC
