@@ -84,7 +84,8 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 
 // Tile choice.  Lanes own 8 elements of a 256-column strip when N > 128
 // (fp32: two 16-byte loads per step; bf16: one); 4 elements of a 128- or
-// 64-column strip for narrower N.  16 warps per CTA.  bf16 steps are
+// 64-column strip for narrower N.  16 warps per CTA (20 for fp32 128-wide
+// strips with 2-4 rows a warp, below).  bf16 steps are
 // latency-bound and run two CTAs per SM (≤ 64 registers, 96 KB of stage
 // each); fp32 steps are bound by shared-memory bandwidth and run one CTA per
 // SM with up to 128 registers and one 192 KB stage (N > 128: KC = 192 rows
@@ -239,9 +240,20 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
         if (a.N <= 128 && groups(128))
             return launch_pick<false, 32, 4, W, 384, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
+        // Warps a CTA.  128-wide strips with 2-4 rows a warp fit in 102
+        // registers, so 20 warps hide more of the loads' latency: LSTM sweep
+        // (N = 128) 3-4% faster at 50-90% sparsity than with 16 (24 warps spill
+        // and are slower).  The sparse-mask shape (up to 8 rows a warp) measured
+        // mixed at 20 (-4..+2.5%) and slower at 24, so it keeps 16.
+#ifndef USM_SPMM_W_N128
+#define USM_SPMM_W_N128 20
+#endif
+#ifndef USM_SPMM_W_HS
+#define USM_SPMM_W_HS 16
+#endif
         if (a.N <= 128) {
-            if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
-            return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
+            if (sparse) return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
+            return launch_pick<false, 32, 4, USM_SPMM_W_N128, 192 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
         }
 #ifndef USM_SPMM_TMEM
 #define USM_SPMM_TMEM 1
@@ -263,7 +275,7 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         if (groups(256)) return launch_pick<false, 32, 8, W, 192, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
         if (!SMX && USM_SPMM_TMEM && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
             return launch_pick<false, 32, 8, W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
-        if (sparse) return launch_pick<false, 32, 4, W, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
+        if (sparse) return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
         return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
     }
     if (a.N <= 64) return launch_pick<true, 16, 4, W, 384 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
