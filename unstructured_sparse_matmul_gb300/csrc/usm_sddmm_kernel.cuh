@@ -12,10 +12,10 @@
 //   K chunks (grid z).  It walks its range in chunks of KC
 //   rows; one thread copies Y[k0:k0+KC, d0:d0+DT] into a shared-memory stage
 //   with TMA (mbarrier, bounded wait) into one tall stage: the tall chunks
-//   halve the per-(row, chunk) work of a double-buffered layout.  bf16 runs
-//   two CTAs per SM with 96 KB each (latency-bound: the two CTAs cover each
-//   other's loads); fp32, bound by shared-memory bandwidth, runs one CTA per
-//   SM with a 192 KB stage and up to 128 registers.
+//   halve the per-(row, chunk) work of a double-buffered layout.  One CTA
+//   per SM with a 192 KB stage: fp32 with 16 warps and up to 128 registers
+//   (24 warps on 128-wide strips), bf16 with 28-32 warps of up to 72
+//   registers (latency-bound: the warps cover each other's loads).
 // * Per (row, chunk) a warp keeps X[r, d0:d0+DT] in registers (fp32), reads
 //   the row's next 32 column indices (coalesced window after its cursor),
 //   keeps the prefix inside the chunk and lists their stage offsets.

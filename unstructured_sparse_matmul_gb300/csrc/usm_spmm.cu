@@ -278,14 +278,38 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         if (sparse) return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
         return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
     }
-    if (a.N <= 64) return launch_pick<true, 16, 4, W, 384 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
+    // bf16 warps and CTAs a SM.  One CTA of 24 or 28 warps with one 192 KB
+    // stage (what the bf16 SDDMM runs) measured even or slower here: FFN bf16
+    // SpMM total -0.3% (28 warps, mixed per launch) and +4% (24); attention
+    // (N = 64) 11-27% slower.  So two CTAs of 16 warps, 96 KB each.
+#ifndef USM_SPMM_BF_W
+#define USM_SPMM_BF_W 16
+#endif
+#ifndef USM_SPMM_BF_MB
+#define USM_SPMM_BF_MB 2
+#endif
+#ifndef USM_SPMM_BF128_W
+#define USM_SPMM_BF128_W 16
+#endif
+#ifndef USM_SPMM_BF128_MB
+#define USM_SPMM_BF128_MB 2
+#endif
+#ifndef USM_SPMM_BF64_W
+#define USM_SPMM_BF64_W 16
+#endif
+#ifndef USM_SPMM_BF64_MB
+#define USM_SPMM_BF64_MB 2
+#endif
+    constexpr int BW = USM_SPMM_BF_W, BMB = USM_SPMM_BF_MB, BW1 = USM_SPMM_BF128_W, BMB1 = USM_SPMM_BF128_MB;
+    constexpr int BW6 = USM_SPMM_BF64_W, BMB6 = USM_SPMM_BF64_MB;
+    if (a.N <= 64) return launch_pick<true, 16, 4, BW6, 768 * F / BMB6, NS, BMB6, 2, 4, false, SMX>(a, B, ldb, stream);
 #ifndef USM_SPMM_HS_BF_PCT
 #define USM_SPMM_HS_BF_PCT 12
 #endif
     // bf16 on sparse masks with long rows of B (K > 2048): 128-wide strips
     // (measured: 1024x4096 at 90% 4% faster, at 95% 12%; 4096x1024 1-8% slower).
     if (a.N <= 128 || (a.K > 2048 && 100LL * a.nnz < (long long)USM_SPMM_HS_BF_PCT * cells))
-        return launch_pick<true, 32, 4, W, 192 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
+        return launch_pick<true, 32, 4, BW1, 384 * F / BMB1, NS, BMB1, 2, 4, false, SMX>(a, B, ldb, stream);
     // 16 bf16 a lane (512-column strips in two TMA boxes, fewer instructions
     // per FMA) measured no faster at 70% and 6-25% slower at 90-95%.
 // bf16 rows in tensor memory (256 columns for each of the two CTAs an SM
@@ -300,7 +324,7 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #endif
     if (!SMX && USM_SPMM_TMEM_BF && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
         return launch_pick<true, 32, 8, W, 96 * F, NS, 2, 2, USM_TM_RB_BF, NS == 1>(a, B, ldb, stream);
-    return launch_pick<true, 32, 8, W, 96 * F, NS, 2, 2, 4, false, SMX>(a, B, ldb, stream);
+    return launch_pick<true, 32, 8, BW, 192 * F / BMB, NS, BMB, 2, 4, false, SMX>(a, B, ldb, stream);
 }
 
 int launch_spmm(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStream_t stream, bool softmax) {
