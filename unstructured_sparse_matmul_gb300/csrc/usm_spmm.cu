@@ -264,15 +264,15 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #ifndef USM_TM_RB
 #define USM_TM_RB 4
 #endif
-        // fp32 256-wide strips of masks at least a quarter set (that row
-        // groups did not take above): the last 64 rows of every chunk also go
-        // to tensor memory (measured on the FFN
-        // launches at 70% sparsity: 5-9% faster; at 80% even; 10-20% slower at
-        // 90-95%, where the copies and their waits are not paid back).
 #ifndef USM_TM_KC
 #define USM_TM_KC (96 * F)
 #endif
         if (groups(256)) return launch_pick<false, 32, 8, W, 192, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
+        // fp32 256-wide strips of masks at least a quarter set (that row groups
+        // did not take above): the last 64 rows of every chunk also go to
+        // tensor memory (measured on the FFN launches at 70% sparsity: 5-9%
+        // faster; at 80% even; 10-20% slower at 90-95%, where the copies and
+        // their waits are not paid back).
         if (!SMX && USM_SPMM_TMEM && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
             return launch_pick<false, 32, 8, W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
         if (sparse) return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
@@ -312,10 +312,10 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         return launch_pick<true, 32, 4, BW1, 384 * F / BMB1, NS, BMB1, 2, 4, false, SMX>(a, B, ldb, stream);
     // 16 bf16 a lane (512-column strips in two TMA boxes, fewer instructions
     // per FMA) measured no faster at 70% and 6-25% slower at 90-95%.
-// bf16 rows in tensor memory (256 columns for each of the two CTAs an SM
-// holds, one tcgen05.ld.x4 a nonzero): measured 8-17% slower at 70% sparsity
-// and even at 80% (two CTAs of 64 registers do not hide the loads' waits),
-// so off by default.
+    // bf16 rows in tensor memory (256 columns for each of the two CTAs an SM
+    // holds, one tcgen05.ld.x4 a nonzero): measured 8-17% slower at 70%
+    // sparsity and even at 80% (two CTAs of 64 registers do not hide the
+    // loads' waits), so off by default.
 #ifndef USM_SPMM_TMEM_BF
 #define USM_SPMM_TMEM_BF 0
 #endif
