@@ -278,15 +278,17 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         if (sparse) return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
         return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
     }
-    // bf16 warps and CTAs a SM.  One CTA of 24 or 28 warps with one 192 KB
-    // stage (what the bf16 SDDMM runs) measured even or slower here: FFN bf16
-    // SpMM total -0.3% (28 warps, mixed per launch) and +4% (24); attention
-    // (N = 64) 11-27% slower.  So two CTAs of 16 warps, 96 KB each.
+    // bf16 warps and CTAs a SM.  256-wide strips: one CTA of 28 warps with one
+    // 192 KB stage (twice the rows sharing each staged chunk, windows fetched
+    // a row slot ahead rather than kept) against two CTAs of 16 with 96 KB
+    // each: measured 2-16% faster on all six FFN launches that take it.
+    // 128-wide strips (6% slower that way) and N <= 64 (attention, 2% slower)
+    // keep two CTAs of 16 warps.
 #ifndef USM_SPMM_BF_W
-#define USM_SPMM_BF_W 16
+#define USM_SPMM_BF_W 28
 #endif
 #ifndef USM_SPMM_BF_MB
-#define USM_SPMM_BF_MB 2
+#define USM_SPMM_BF_MB 1
 #endif
 #ifndef USM_SPMM_BF128_W
 #define USM_SPMM_BF128_W 16
