@@ -282,8 +282,9 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
     // 192 KB stage (twice the rows sharing each staged chunk, windows fetched
     // a row slot ahead rather than kept) against two CTAs of 16 with 96 KB
     // each: measured 2-16% faster on all six FFN launches that take it.
-    // 128-wide strips (6% slower that way) and N <= 64 (attention, 2% slower)
-    // keep two CTAs of 16 warps.
+    // 128-wide strips (6% slower that way; 12% with one CTA of 20 warps that
+    // keeps its windows) and N <= 64 (attention, 2% and 28% slower) keep two
+    // CTAs of 16 warps.
 #ifndef USM_SPMM_BF_W
 #define USM_SPMM_BF_W 28
 #endif
