@@ -273,10 +273,21 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         // tensor memory (measured on the FFN launches at 70% sparsity: 5-9%
         // faster; at 80% even; 10-20% slower at 90-95%, where the copies and
         // their waits are not paid back).
+        // 256-wide strips without tensor-memory rows: 20 warps, the CSR windows
+        // fetched a row slot ahead rather than kept (which leaves no spills),
+        // against 16 warps with kept windows: FFN 4096x1024 4-7% faster at
+        // 80-90% sparsity, 1024x4096 1% slower.  The tensor-memory shape needs
+        // its 128 registers at 16 warps (32 warps of 2 rows spill).
+#ifndef USM_TM_W
+#define USM_TM_W 16
+#endif
+#ifndef USM_SPMM_W256
+#define USM_SPMM_W256 20
+#endif
         if (!SMX && USM_SPMM_TMEM && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
-            return launch_pick<false, 32, 8, W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
+            return launch_pick<false, 32, 8, USM_TM_W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
         if (sparse) return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
-        return launch_pick<false, 32, 8, W, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
+        return launch_pick<false, 32, 8, USM_SPMM_W256, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
     }
     // bf16 warps and CTAs a SM.  256-wide strips: one CTA of 28 warps with one
     // 192 KB stage (twice the rows sharing each staged chunk, windows fetched

@@ -344,16 +344,14 @@ __global__ void __launch_bounds__(W * 32, MB)
     }
 
     int cur = my_start;  // lane i: cursor of row slot i
-    // PERSIST (one CTA per SM of at most 20 warps, registers to spare): each
-    // row slot keeps a 32-entry window of its CSR arrays in registers across
-    // chunks (lane e holds entry wb[i] + e), so at high sparsity one window
-    // serves several chunks.  Otherwise (two CTAs per SM, or one of 28 warps:
-    // 64-72 registers, where the kept windows would spill) the window of the
-    // next row slot is fetched while the current one computes.
-#ifndef USM_PERSIST_MAX_THREADS
-#define USM_PERSIST_MAX_THREADS 640
-#endif
-    constexpr bool PERSIST = MB == 1 && W * 32 <= USM_PERSIST_MAX_THREADS;
+    // PERSIST (one CTA per SM with registers to spare: up to 20 warps with 4
+    // elements a lane, 16 with 8): each row slot keeps a 32-entry window of
+    // its CSR arrays in registers across chunks (lane e holds entry wb[i] +
+    // e), so at high sparsity one window serves several chunks.  Otherwise
+    // (two CTAs per SM, or larger CTAs, where the kept windows would spill)
+    // the window of the next row slot is fetched while the current one
+    // computes.
+    constexpr bool PERSIST = MB == 1 && W * 32 <= (VEC <= 4 ? 640 : 512);
     constexpr int RW = PERSIST ? R : 1;
     int wcol[RW];
     uint32_t wval[RW];
