@@ -200,9 +200,12 @@ int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, si
         // 11-12% at 95%; 20 and 32 warps gained less.  (256-wide strips, 96
         // registers at 20 warps: no change, those launches are bound by
         // shared-memory bandwidth.)
+        // Launch-bound problems (one or two CTAs: the 256x256 mask at 90%, 4.2
+        // against 4.6 us a call) keep 16 warps, whose set-up is shorter.
 #ifndef USM_SDDMM_W128
 #define USM_SDDMM_W128 24
 #endif
+        if (a.nnz < 100000) return launch_cfg<false, 8, 4, W, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
         return launch_cfg<false, 8, 4, USM_SDDMM_W128, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
     }
     // bf16: one CTA a SM of 28 warps (D > 64; 64-72 registers) or 32 (D <= 64;
