@@ -219,8 +219,8 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         // 64-row tiles cover under half the SMs (2048x2048, N = 512: 26% slower).
         // 64 < N <= 128 takes 128-column strips, where each column carries half
         // the FMAs for the same list work: 8192x4096, N = 128, 50% density even,
-        // 60% 13% faster, 70% 28%, 90% 54%; 40% density 9% slower; so from
-        // 55% there.  K <= 6144 keeps its rounding bound.  The choice depends
+        // 60% 9% faster, 70% 23%, 90% 49%; 40% density 9% slower; so from 55%
+        // there.  K <= 6144 keeps its rounding bound.  The choice depends
         // on M, N, K, nnz only, never on the schedule arguments.
 #ifndef USM_SPMM_GROUP
 #define USM_SPMM_GROUP 1
