@@ -276,10 +276,14 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         // 256-wide strips without tensor-memory rows: 20 warps, the CSR windows
         // fetched a row slot ahead rather than kept (which leaves no spills),
         // against 16 warps with kept windows: FFN 4096x1024 4-7% faster at
-        // 80-90% sparsity, 1024x4096 1% slower.  The tensor-memory shape needs
-        // its 128 registers at 16 warps (32 warps of 2 rows spill).
+        // 80-90% sparsity, 1024x4096 1% slower.  The tensor-memory shape runs
+        // 18 warps at 96 registers (five warps on a subpartition, as with 20;
+        // the CSR windows fetched a row slot ahead): FFN at 70% sparsity 3%
+        // (1024x4096) and 9% (4096x1024) faster than 16 warps at 128 registers,
+        // 1024x4096 at 50% 5%; 20 warps ran the same or up to 1% slower; 24
+        // (80 registers, spilling) 11% slower than 16 on 1024x4096.
 #ifndef USM_TM_W
-#define USM_TM_W 16
+#define USM_TM_W 18
 #endif
 #ifndef USM_SPMM_W256
 #define USM_SPMM_W256 20

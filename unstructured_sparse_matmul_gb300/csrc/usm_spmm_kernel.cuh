@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(W * 32, MB)
     constexpr int KL = KC - TR;  // chunk rows read from shared memory
     constexpr int TCPR = BF ? 4 : 8;         // tensor-memory columns a row
     constexpr uint32_t TCOLS = BF ? 256 : 512;  // columns allocated
-    static_assert(!TM || (L == 32 && VEC == 8 && NS == 1 && MB == (BF ? 2 : 1) && KC > TR && TR % W == 0 &&
+    static_assert(!TM || (L == 32 && VEC == 8 && NS == 1 && MB == (BF ? 2 : 1) && KC > TR && TR >= W &&
                           TR * TCPR == (int)TCOLS),
                   "tensor-memory rows: 32 lanes x 16 or 32 bytes, one stage, 1 (fp32) or 2 (bf16) CTAs per SM");
     static_assert(!VL || (G == 1 && !TM), "vector windows: one lane group, no tensor-memory rows");
@@ -397,12 +397,13 @@ __global__ void __launch_bounds__(W * 32, MB)
         const uint32_t stage = stage0 + lane_off;
         bool tm_ready = false, tm_failed = false;  // TM: this chunk's tensor-memory rows have landed
         if constexpr (TM) {
-            // The chunk is in shared memory: each warp copies its TR/W rows of
+            // The chunk is in shared memory: warp w copies rows w, w + W, ... of
             // the tensor-memory part (two 512-byte halves a row) and commits.
             if (ok && lane == 0) {
 #pragma unroll
-                for (int q = 0; q < TR / W; ++q) {
-                    const int rr = warp * (TR / W) + q;
+                for (int q = 0; q < (TR + W - 1) / W; ++q) {
+                    const int rr = warp + q * W;
+                    if (rr >= TR) break;
                     tmem_cp_512b_x4((uint32_t)kr[3] + TCPR * rr, stage0 + (KL + rr) * PITCH);
                     if (!BF) tmem_cp_512b_x4((uint32_t)kr[3] + TCPR * rr + 4, stage0 + (KL + rr) * PITCH + 512);
                 }
