@@ -147,9 +147,10 @@ def test_spmm_leading_dimensions(usm):
 
 
 @pytest.mark.parametrize("M,K,N,density,seg", [(900, 500, 300, 0.4, 0), (700, 2500, 257, 0.3, 0),
-                                                (1000, 1000, 512, 0.6, 500), (300, 4097, 600, 0.3, 0)])
+                                                (1000, 1000, 512, 0.6, 500), (300, 4097, 600, 0.3, 0),
+                                                (800, 1500, 300, 0.17, 0)])
 def test_spmm_tensor_memory_rows(usm, schedule, M, K, N, density, seg):
-    """fp32 masks at least a quarter set with N > 128 read the last 64 rows
+    """fp32 masks at least 15% set with N > 128 read the last 64 rows
     of every 192-row chunk from tensor memory: ragged last chunks (K not a
     multiple of 192: some of those rows lie past K), several and ragged
     strips, block-diagonal schedules and forced schedules, every element
@@ -163,7 +164,7 @@ def test_spmm_tensor_memory_rows(usm, schedule, M, K, N, density, seg):
         csr = W.CSR(M, K, ro, ci, W.values_for(rng, int(ro[-1]), 1.0, "f32"), "f32", seg_rows=seg)
     else:
         csr = W.random_csr([M, K, N, 152], M, K, density)
-    assert csr.nnz >= 0.25 * M * K
+    assert csr.nnz >= 0.15 * M * K
     B = W.dense(np.random.default_rng([M, K, 153]), K, N)
     rod, cid, vd = csr_dev(csr)
     Bd = dev(B)

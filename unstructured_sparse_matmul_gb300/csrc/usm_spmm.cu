@@ -259,7 +259,7 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #define USM_SPMM_TMEM 1
 #endif
 #ifndef USM_TM_MIN_DENSITY_PCT
-#define USM_TM_MIN_DENSITY_PCT 25
+#define USM_TM_MIN_DENSITY_PCT 15
 #endif
 #ifndef USM_TM_RB
 #define USM_TM_RB 4
@@ -268,11 +268,14 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #define USM_TM_KC (96 * F)
 #endif
         if (groups(256)) return launch_pick<false, 32, 8, W, 192, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
-        // fp32 256-wide strips of masks at least a quarter set (that row groups
-        // did not take above): the last 64 rows of every chunk also go to
-        // tensor memory (measured on the FFN launches at 70% sparsity: 5-9%
-        // faster; at 80% even; 10-20% slower at 90-95%, where the copies and
-        // their waits are not paid back).
+        // fp32 256-wide strips of masks at least 15% set (that row groups did
+        // not take above): the last 64 rows of every chunk also go to tensor
+        // memory.  Measured on the FFN launches: at 70% sparsity 6-8% faster
+        // than shared memory alone (both at 16 warps; 18 warps then gained
+        // another 3-10%); at 18 warps against the 20-warp shape below, 80%
+        // 3-4% faster and 90% 5% slower (the copies and their waits are not
+        // paid back), so the threshold sits between the two.  ResNet's
+        // 512x2048 at 80% (N = 3136) measured 1% slower.
         // 256-wide strips without tensor-memory rows: 20 warps, the CSR windows
         // fetched a row slot ahead rather than kept (which leaves no spills),
         // against 16 warps with kept windows: FFN 4096x1024 4-7% faster at
