@@ -94,7 +94,7 @@ WORKLOADS = {
     "lstm": "LSTM-sized sweep, fp32: A 8192x4096 at 50/60/70/80/90/95/98%, B 4096x128, SpMM only",
     "dense_masks": "denser masks, fp32 SpMM only: the FFN shapes (A 4096x1024 and 1024x4096, B Kx2048) at "
                    "20/30/40/50% sparsity and the LSTM shape (A 8192x4096, B 4096x128) at 10/20/30/40% (masks at "
-                   "least half set, or 55% with N <= 128, run the row-group kernel)",
+                   "least 55% set run the row-group kernel)",
     "resnet": "ResNet-50-like 1x1 conv, fp32: A 512x2048 at 80%, B 2048x3136 SpMM and SDDMM weight-gradient "
               "(X 512x3136, Y 2048x3136); L2 flushed before every step",
     "tiny": "tiny parity config, fp32: A 256x256 at 90%, B/X/Y 256x64, SpMM and SDDMM; launch-bound, so each "

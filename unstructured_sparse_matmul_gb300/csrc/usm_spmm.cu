@@ -210,31 +210,28 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         // at the same registers.  Measured against 256-wide strips with up to 4
         // rows a warp: FFN 95% 6-11% faster, 90% -2..+3%, LSTM even.
         const bool sparse = 100LL * a.nnz < (long long)USM_SPMM_HS_PCT * cells;
-        // fp32 masks at least half set: row groups (usm_spmm_group.cuh), where
+        // fp32 masks at least 55% set: row groups (usm_spmm_group.cuh), where
         // a staged row of B serves all of a warp's rows holding its column.
-        // Measured against the row kernel (N = 2048, one stream): 1024x4096
-        // at 50% density 4% faster, 60% 15%, 80% 40%; 4096x1024 at 60% 16%;
-        // 30-40% density 5-17% slower (the predicated FMAs of the rows without
-        // a column cost more than the loads saved), and so are grids whose
-        // 64-row tiles cover under half the SMs (2048x2048, N = 512: 26% slower).
-        // 64 < N <= 128 takes 128-column strips, where each column carries half
-        // the FMAs for the same list work: 8192x4096, N = 128, 50% density even,
-        // 60% 9% faster, 70% 23%, 90% 49%; 40% density 9% slower; so from 55%
-        // there.  K <= 6144 keeps its rounding bound.  The choice depends
-        // on M, N, K, nnz only, never on the schedule arguments.
+        // Measured against the row kernel with tensor-memory rows (N = 2048,
+        // one stream): 60% density 5% (4096x1024) and 9% (1024x4096) faster
+        // (80%: 40%, against 16 warps); 50% density 5% slower (4096x1024);
+        // 30-40% slower still (the predicated FMAs of the rows without a
+        // column cost more than the loads saved), and so are grids whose
+        // 64-row tiles cover under half the SMs (2048x2048, N = 512: 26%
+        // slower).  64 < N <= 128 takes 128-column strips, where each column
+        // carries half the FMAs for the same list work: 8192x4096, N = 128,
+        // 50% density even, 60% 9% faster, 70% 23%, 90% 49%; 40% density 9%
+        // slower.  K <= 6144 keeps its rounding bound.  The choice depends on
+        // M, N, K, nnz only, never on the schedule arguments.
 #ifndef USM_SPMM_GROUP
 #define USM_SPMM_GROUP 1
 #endif
 #ifndef USM_GROUP_MIN_PCT
-#define USM_GROUP_MIN_PCT 50
-#endif
-#ifndef USM_GROUP_MIN_PCT_N128
-#define USM_GROUP_MIN_PCT_N128 55
+#define USM_GROUP_MIN_PCT 55
 #endif
         auto groups = [&](int strip) {
             const long long ctas = (long long)((a.M + 63) / 64) * ((a.N + strip - 1) / strip);
-            const long long pct = strip == 128 ? USM_GROUP_MIN_PCT_N128 : USM_GROUP_MIN_PCT;
-            return USM_SPMM_GROUP && NS == 1 && a.K <= 6144 && 100LL * a.nnz >= pct * cells &&
+            return USM_SPMM_GROUP && NS == 1 && a.K <= 6144 && 100LL * a.nnz >= USM_GROUP_MIN_PCT * cells &&
                    2 * ctas >= sm_count_current_device();
         };
         if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);

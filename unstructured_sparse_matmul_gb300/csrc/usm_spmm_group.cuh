@@ -1,5 +1,5 @@
-// CSR SpMM on row groups (fp32, 256-column strips), for masks at least
-// half set.
+// CSR SpMM on row groups (fp32, 256- or 128-column strips), for masks at
+// least 55% set.
 //
 // "Sparse GPU Kernels for Deep Learning" (Gale et al., SC 2020), summary
 // card "Summary": SpMM on plain CSR with 1-D row tiles.  The row-at-a-time
