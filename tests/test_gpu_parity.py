@@ -151,8 +151,9 @@ def test_spmm_leading_dimensions(usm):
                                                 (800, 1500, 300, 0.17, 0)])
 def test_spmm_tensor_memory_rows(usm, schedule, M, K, N, density, seg):
     """fp32 masks at least 15% set with N > 128 read the last 64 rows
-    of every 192-row chunk from tensor memory: ragged last chunks (K not a
-    multiple of 192: some of those rows lie past K), several and ragged
+    of every chunk from tensor memory, with chunks of 192 rows (K = 500,
+    1500) and 208 (K = 1000, 2500, 4097: fewer chunks): ragged last chunks
+    (some of those rows lie past K), several and ragged
     strips, block-diagonal schedules and forced schedules, every element
     against the oracle and forced schedules bit for bit."""
     if seg:
@@ -307,7 +308,7 @@ def test_spmm_non_finite_b_reaches_only_its_rows(usm, density):
 
 
 def test_spmm_long_k_fp32(usm):
-    """fp32 with more than 128 chunks of K (K = 40000: 209 chunks of 192
+    """fp32 with more than 128 chunks of K (K = 40000: 193 chunks of 208
     rows) takes the kernel with a second-level accumulator; with every
     value and every B element positive the rounding errors cannot cancel,
     and each element must still be within 1e-5 of its error scale."""

@@ -18,6 +18,14 @@ constexpr unsigned kFullMask = 0xffffffffu;
 // returns instead of spinning forever.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Rows of one TMA box for a chunk of kc staged rows: the largest divisor of kc
+// that is at most 256 (a box dimension's limit), so whole boxes tile the chunk.
+constexpr int tma_box_rows(int kc) {
+    for (int b = kc < 256 ? kc : 256; b > 1; --b)
+        if (kc % b == 0) return b;
+    return 1;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

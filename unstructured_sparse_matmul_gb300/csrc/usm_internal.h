@@ -39,6 +39,13 @@ int* status_word_for_current_device();
 // Number of SMs of the current device (cached per device).
 int sm_count_current_device();
 
+// Whether chunks of kc_tall staged rows walk K in fewer chunks than chunks of
+// kc.  A taller chunk means fewer CTA barriers and refills, but when it saves
+// no chunk it only stages more rows past K (zero-filled by the copy).
+inline bool taller_chunk_pays(int K, int kc, int kc_tall) {
+    return (K + kc_tall - 1) / kc_tall < (K + kc - 1) / kc;
+}
+
 // Encode a 2-D row-major tensor map (inner dim = cols) with box
 // {box_cols, box_rows}.  Returns false if the driver entry point is missing
 // or the encode fails.

@@ -182,8 +182,9 @@ int launch_fill_out(void* out, long long n, bool bf16, cudaStream_t stream) {
 int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, size_t ws_bytes,
                  cudaStream_t stream) {
     constexpr int W = 16, NS = USM_SDDMM_STAGES, F = 2 / NS;  // F: chunk growth with one stage
-    // fp32: one CTA per SM, up to 128 registers, one 192 KB stage (KC = 384
-    // rows of a 128-wide strip, or 192 of a 256-wide one).
+    // fp32: one CTA per SM, up to 128 registers, one stage of 192 KB or more
+    // (KC = 384 or 416 rows of a 128-wide strip, 192 or 216 of a 256-wide
+    // one).
     if (!in_bf16) {
         // 256-wide strips (masks at least a quarter set); USM_SDDMM_TMEM=1 also
         // reads the last 64 rows of every chunk from tensor memory.
@@ -192,8 +193,20 @@ int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, si
 #ifndef USM_SDDMM_TMEM
 #define USM_SDDMM_TMEM 0
 #endif
-        if (strip_width(a.M, a.K, a.D, a.nnz, false) == 256)
-            return launch_cfg<false, 8, 8, W, 96 * F, 1, NS, USM_SDDMM_TMEM && NS == 1>(a, Y, ldy, ws, ws_bytes, stream);
+        // Chunk rows: 216 (a 216 KB stage, what the shared memory leaves beside
+        // the lists) where that saves a chunk against 192: 2-3% faster on the
+        // FFN launches at 70% sparsity; 224 ran the same or slower.  The
+        // results do not depend on the chunk height (each nonzero is one dot
+        // product over the strip).
+#ifndef USM_SDDMM_KC256
+#define USM_SDDMM_KC256 (108 * F)
+#endif
+        if (strip_width(a.M, a.K, a.D, a.nnz, false) == 256) {
+            constexpr bool TM = USM_SDDMM_TMEM && NS == 1;
+            if (taller_chunk_pays(a.K, 96 * F, USM_SDDMM_KC256))
+                return launch_cfg<false, 8, 8, W, USM_SDDMM_KC256, 1, NS, TM>(a, Y, ldy, ws, ws_bytes, stream);
+            return launch_cfg<false, 8, 8, W, 96 * F, 1, NS, TM>(a, Y, ldy, ws, ws_bytes, stream);
+        }
         // 128-wide strips hold half the X registers (80 a thread at 24 warps):
         // 24 warps hide more of the loads' latency.  Measured against 16 on the
         // FFN launches (80-95% sparsity): 5-6% faster at 80%, 9% at 90%,
@@ -205,7 +218,15 @@ int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, si
 #ifndef USM_SDDMM_W128
 #define USM_SDDMM_W128 24
 #endif
+        // Chunk rows: 416 where that saves a chunk against 384 (FFN 1024x4096
+        // at 80-95% sparsity 1.5-5% faster; with K = 1024, where it saves none,
+        // 1-3% slower).
+#ifndef USM_SDDMM_KC128
+#define USM_SDDMM_KC128 (208 * F)
+#endif
         if (a.nnz < 100000) return launch_cfg<false, 8, 4, W, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
+        if (taller_chunk_pays(a.K, 192 * F, USM_SDDMM_KC128))
+            return launch_cfg<false, 8, 4, USM_SDDMM_W128, USM_SDDMM_KC128, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
         return launch_cfg<false, 8, 4, USM_SDDMM_W128, 192 * F, 1, NS>(a, Y, ldy, ws, ws_bytes, stream);
     }
     // bf16: one CTA a SM of 28 warps (D > 64; 64-72 registers) or 32 (D <= 64;
@@ -228,8 +249,22 @@ int launch_sddmm(SddmmArgs a, const void* Y, int ldy, bool in_bf16, void* ws, si
 #endif
     constexpr int BW = USM_SDDMM_BF_W, BMB = USM_SDDMM_BF_MB, SW = USM_SDDMM_BF64_W, SMB = USM_SDDMM_BF64_MB;
     if (a.D <= 64) return launch_cfg<true, 8, 1, SW, 768 * F / SMB, SMB, NS>(a, Y, ldy, ws, ws_bytes, stream);
-    if (strip_width(a.M, a.K, a.D, a.nnz, true) == 256)
+    // Chunk rows: 416 (256-wide strips) and 832 (128-wide) where that saves a
+    // chunk against 384 and 768: FFN 1024x4096 at 70% 1.6% faster, 80% 6%,
+    // 90% 2.5%, 95% even (432 and 864 the same).
+#ifndef USM_SDDMM_BF_KC_TALL
+#define USM_SDDMM_BF_KC_TALL (208 * F / BMB)
+#endif
+#ifndef USM_SDDMM_BF128_KC_TALL
+#define USM_SDDMM_BF128_KC_TALL (416 * F / BMB)
+#endif
+    if (strip_width(a.M, a.K, a.D, a.nnz, true) == 256) {
+        if (taller_chunk_pays(a.K, 192 * F / BMB, USM_SDDMM_BF_KC_TALL))
+            return launch_cfg<true, 8, 4, BW, USM_SDDMM_BF_KC_TALL, BMB, NS>(a, Y, ldy, ws, ws_bytes, stream);
         return launch_cfg<true, 8, 4, BW, 192 * F / BMB, BMB, NS>(a, Y, ldy, ws, ws_bytes, stream);
+    }
+    if (taller_chunk_pays(a.K, 384 * F / BMB, USM_SDDMM_BF128_KC_TALL))
+        return launch_cfg<true, 8, 2, BW, USM_SDDMM_BF128_KC_TALL, BMB, NS>(a, Y, ldy, ws, ws_bytes, stream);
     return launch_cfg<true, 8, 2, BW, 384 * F / BMB, BMB, NS>(a, Y, ldy, ws, ws_bytes, stream);
 }
 

@@ -13,7 +13,7 @@
 //   rows; one thread copies Y[k0:k0+KC, d0:d0+DT] into a shared-memory stage
 //   with TMA (mbarrier, bounded wait) into one tall stage: the tall chunks
 //   halve the per-(row, chunk) work of a double-buffered layout.  One CTA
-//   per SM with a 192 KB stage: fp32 with 16 warps and up to 128 registers
+//   per SM with a stage of 192-216 KB: fp32 with 16 warps and up to 128 registers
 //   (24 warps on 128-wide strips), bf16 with 28-32 warps of up to 72
 //   registers (latency-bound: the warps cover each other's loads).
 // * Per (row, chunk) a warp keeps X[r, d0:d0+DT] in registers (fp32), reads
@@ -65,7 +65,7 @@ struct SddmmCfg {
     static constexpr int G = 32 / L;
     static constexpr int PITCH = L * VV * 16;   // bytes per staged Y row
     static constexpr int STAGE = KC * PITCH;
-    static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
+    static constexpr int BOX_ROWS = tma_box_rows(KC);
     static constexpr int THREADS = W * 32;
     static constexpr int SMEM = NS * STAGE + 64 + W * 32 * 4;
     static constexpr int XW = VV * 4;           // 32-bit words of X per lane

@@ -88,8 +88,9 @@ int launch_fill_f32(float* C, int M, int N, long long ldc, cudaStream_t stream) 
 // strips with 2-4 rows a warp, below).  bf16 steps are
 // latency-bound and run two CTAs per SM (≤ 64 registers, 96 KB of stage
 // each); fp32 steps are bound by shared-memory bandwidth and run one CTA per
-// SM with up to 128 registers and one 192 KB stage (N > 128: KC = 192 rows
-// of 1 KB; N ≤ 128: 384 rows of 512 B; N ≤ 64: 768 of 256 B): taller chunks
+// SM with up to 128 registers and one stage of 192 KB or more (N > 128: KC =
+// 192 or 208 rows of 1 KB; N ≤ 128: 384 or 416 rows of 512 B; N ≤ 64: 768 of
+// 256 B; the taller where it saves a chunk): taller chunks
 // halve the per-(row, chunk) work and more rows per CTA share each staged
 // row, and row slots keep their CSR windows across chunks.  Measured against
 // two CTAs per SM: FFN fp32 SpMM 3-12% faster, LSTM (N = 128) 5% faster at
@@ -248,8 +249,23 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #ifndef USM_SPMM_W_HS
 #define USM_SPMM_W_HS 16
 #endif
+        // Chunk rows of the 128-wide shapes: 416 where that saves a chunk
+        // against 384 (K = 4096: LSTM at 90-95% sparsity and FFN 1024x4096 at
+        // 95% 2-3% faster; with K = 1024, where it saves none, 1-2% slower).
+#ifndef USM_SPMM_KC128
+#define USM_SPMM_KC128 (208 * F)
+#endif
+        const bool tall128 = taller_chunk_pays(a.K, 192 * F, USM_SPMM_KC128);
+        auto sparse_shape = [&]() {
+            if (tall128)
+                return launch_pick<false, 32, 4, USM_SPMM_W_HS, USM_SPMM_KC128, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
+            return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
+        };
         if (a.N <= 128) {
-            if (sparse) return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
+            if (sparse) return sparse_shape();
+            if (tall128)
+                return launch_pick<false, 32, 4, USM_SPMM_W_N128, USM_SPMM_KC128, NS, 1, 2, 4, false, SMX>(a, B, ldb,
+                                                                                                        stream);
             return launch_pick<false, 32, 4, USM_SPMM_W_N128, 192 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
         }
 #ifndef USM_SPMM_TMEM
@@ -260,9 +276,6 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #endif
 #ifndef USM_TM_RB
 #define USM_TM_RB 4
-#endif
-#ifndef USM_TM_KC
-#define USM_TM_KC (96 * F)
 #endif
         if (groups(256)) return launch_pick<false, 32, 8, W, 192, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
         // fp32 256-wide strips of masks at least 15% set (that row groups did
@@ -288,9 +301,23 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #ifndef USM_SPMM_W256
 #define USM_SPMM_W256 20
 #endif
-        if (!SMX && USM_SPMM_TMEM && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
-            return launch_pick<false, 32, 8, USM_TM_W, USM_TM_KC, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
-        if (sparse) return launch_pick<false, 32, 4, USM_SPMM_W_HS, 192 * F, NS, 1, 4, 8, false, SMX>(a, B, ldb, stream);
+        // Chunk rows of the 256-wide shapes: 208 (a 208 KB stage, what the
+        // shared memory leaves beside the lists) where that saves a chunk
+        // against 192: 1-4% faster on the FFN launches at 80-90% sparsity and
+        // about 1% with tensor-memory rows at 70-80% (ResNet 2%).
+#ifndef USM_SPMM_KC256
+#define USM_SPMM_KC256 (104 * F)
+#endif
+        const bool tall256 = taller_chunk_pays(a.K, 96 * F, USM_SPMM_KC256);
+        if (!SMX && USM_SPMM_TMEM && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells) {
+            if (tall256)
+                return launch_pick<false, 32, 8, USM_TM_W, USM_SPMM_KC256, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb,
+                                                                                                      stream);
+            return launch_pick<false, 32, 8, USM_TM_W, 96 * F, NS, 1, 2, USM_TM_RB, NS == 1>(a, B, ldb, stream);
+        }
+        if (sparse) return sparse_shape();
+        if (tall256)
+            return launch_pick<false, 32, 8, USM_SPMM_W256, USM_SPMM_KC256, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
         return launch_pick<false, 32, 8, USM_SPMM_W256, 96 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
     }
     // bf16 warps and CTAs a SM.  256-wide strips: one CTA of 28 warps with one
@@ -342,6 +369,9 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #endif
     if (!SMX && USM_SPMM_TMEM_BF && NS == 1 && 100LL * a.nnz >= (long long)USM_TM_MIN_DENSITY_PCT * cells)
         return launch_pick<true, 32, 8, W, 96 * F, NS, 2, 2, USM_TM_RB_BF, NS == 1>(a, B, ldb, stream);
+    // (Chunks of 416 or 432 rows where they save a chunk, as the fp32 shapes
+    // and the bf16 SDDMM take: FFN 1024x4096 at 70-95% sparsity 1% faster to
+    // 2% slower, so 384.)
     return launch_pick<true, 32, 8, BW, 192 * F / BMB, NS, BMB, 2, 4, false, SMX>(a, B, ldb, stream);
 }
 

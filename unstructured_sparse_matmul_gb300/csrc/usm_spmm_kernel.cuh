@@ -78,7 +78,7 @@ struct SpmmCfg {
     static constexpr int NW = LANE_BYTES / 4;      // 32-bit words per lane per step
     static constexpr int BOX_BYTES = KC * PITCH;
     static constexpr int STAGE = NBOX * BOX_BYTES;
-    static constexpr int BOX_ROWS = KC <= 256 ? KC : (KC % 256 == 0 ? 256 : (KC % 192 == 0 ? 192 : 128));
+    static constexpr int BOX_ROWS = tma_box_rows(KC);
     static constexpr int THREADS = W * 32;
     // List entries.  fp32: (stage offset, value bits), 8 bytes.  bf16 with
     // 8-byte lane slices (ADDR): an array of shared-memory row addresses and
