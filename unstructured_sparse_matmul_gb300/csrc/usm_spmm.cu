@@ -347,14 +347,24 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
 #endif
     constexpr int BW = USM_SPMM_BF_W, BMB = USM_SPMM_BF_MB, BW1 = USM_SPMM_BF128_W, BMB1 = USM_SPMM_BF128_MB;
     constexpr int BW6 = USM_SPMM_BF64_W, BMB6 = USM_SPMM_BF64_MB;
+    // (N <= 64 with 832-row chunks where they save a chunk: the attention
+    // SpMM 0.6-1.6% slower, so 768.)
     if (a.N <= 64) return launch_pick<true, 16, 4, BW6, 768 * F / BMB6, NS, BMB6, 2, 4, false, SMX>(a, B, ldb, stream);
+    // 128-wide strips (two CTAs of 96 KB): 416-row chunks where they save a
+    // chunk against 384 (104 KB each), FFN 1024x4096 at 90-95% 2-3% faster.
+#ifndef USM_SPMM_BF128_KC_TALL
+#define USM_SPMM_BF128_KC_TALL (416 * F / BMB1)
+#endif
 #ifndef USM_SPMM_HS_BF_PCT
 #define USM_SPMM_HS_BF_PCT 12
 #endif
     // bf16 on sparse masks with long rows of B (K > 2048): 128-wide strips
     // (measured: 1024x4096 at 90% 4% faster, at 95% 12%; 4096x1024 1-8% slower).
-    if (a.N <= 128 || (a.K > 2048 && 100LL * a.nnz < (long long)USM_SPMM_HS_BF_PCT * cells))
+    if (a.N <= 128 || (a.K > 2048 && 100LL * a.nnz < (long long)USM_SPMM_HS_BF_PCT * cells)) {
+        if (taller_chunk_pays(a.K, 384 * F / BMB1, USM_SPMM_BF128_KC_TALL))
+            return launch_pick<true, 32, 4, BW1, USM_SPMM_BF128_KC_TALL, NS, BMB1, 2, 4, false, SMX>(a, B, ldb, stream);
         return launch_pick<true, 32, 4, BW1, 384 * F / BMB1, NS, BMB1, 2, 4, false, SMX>(a, B, ldb, stream);
+    }
     // 16 bf16 a lane (512-column strips in two TMA boxes, fewer instructions
     // per FMA) measured no faster at 70% and 6-25% slower at 90-95%.
     // bf16 rows in tensor memory (256 columns for each of the two CTAs an SM
