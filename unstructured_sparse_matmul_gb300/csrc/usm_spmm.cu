@@ -238,8 +238,9 @@ int launch_shape(const SpmmArgs& a, const void* B, int ldb, bool bf16, cudaStrea
         if (a.N <= 64) return launch_pick<false, 16, 4, W, 384 * F, NS, 1, 2, 4, false, SMX>(a, B, ldb, stream);
         if (a.N <= 128 && groups(128))
             return launch_pick<false, 32, 4, W, 384, 1, 1, 2, 4, false, SMX, true>(a, B, ldb, stream);
-        // Warps a CTA.  128-wide strips with 2-4 rows a warp fit in 102
-        // registers, so 20 warps hide more of the loads' latency: LSTM sweep
+        // Warps a CTA.  128-wide strips with 2-4 rows a warp need 69-87
+        // registers, under the 96 that 20 warps leave (five on a subpartition
+        // of 16K registers), so 20 warps hide more of the loads' latency: LSTM sweep
         // (N = 128) 3-4% faster at 50-90% sparsity than with 16 (24 warps spill
         // and are slower).  The sparse-mask shape (up to 8 rows a warp) measured
         // mixed at 20 (-4..+2.5%) and slower at 24, so it keeps 16.
